@@ -1,0 +1,430 @@
+"""Benchmark of the packed-Trellis decode-and-multiply on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one fused decode-and-multiply call (trellis_gemm: code fetch,
+window, hash, quotient, scale/bf16 round, M-row FMA, reduction and bf16 store)
+on the headline workload: M=8 activation rows, K=5120, N=17408, k=3 bits, L=12,
+T=256, seeded synthetic inputs.  Metric: packed-weight GB/s (code bytes per
+second, whole job); the JSON line also carries us/call and the roofline
+fraction of the kernel.
+
+Timing: W warm-up steps, then K steps bracketed by a barrier and
+torch.cuda.synchronize(), CUDA events on the launching stream around every
+call, max over ranks.  Between steps the code buffers rotate through enough
+independent copies that the set exceeds twice the L2, so every call streams
+its codes from HBM.  GPU clocks are sampled with nvidia-smi during the timed
+region.  Multi-GPU runs (torchrun) are independent replicas of the workload,
+one per rank (weak scaling, no data-path collective).
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+on a bounded sample of the same workload; it is a deliberately slow baseline.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "gemm_m8_k5120_n17408_k3"
+METRIC = "trellis GEMM packed-weight GB/s"
+DECODE_OPS_PER_WEIGHT = 10        # algorithmic integer/fp32 ops per decoded weight
+ALU_LANES_PER_SM = 128            # 4 sub-partitions x 32 lanes, one op per lane per clock
+
+
+# ----------------------------------------------------------------- helpers --
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "trellis_quantized_weight_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/, if the
+    capture was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                key, val = line[2:].split(":", 1)
+                vals[key.strip()] = val.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(self.period_ms / 1000.0 * 2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def to_dev(bits: np.ndarray, torch, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).cuda()
+
+
+# ------------------------------------------------------------- CPU oracle --
+def oracle_throughput(wl, x, codes, scales, budget_s: float, threads: int, max_rows: int | None = None):
+    """Run the unchanged oracle (decode + product) over row chunks on `threads`
+    host threads for about budget_s seconds; returns (GB/s of codes, rows, s)."""
+    import oracle
+    o = oracle.get()
+    rows_total = wl.N if max_rows is None else min(wl.N, max_rows)
+    chunk = max(1, min(rows_total, 64))
+
+    def work(r):
+        w = o.decode(codes, scales, wl.K, wl.N, wl.k, rows=r)
+        o.gemm_dense(x, w)
+        return r[1] - r[0]
+
+    done_rows = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        n0 = 0
+        while True:
+            batch = []
+            for _ in range(threads):
+                n1 = min(rows_total, n0 + chunk)
+                batch.append((n0, n1))
+                n0 = 0 if n1 >= rows_total else n1
+            done_rows += sum(ex.map(work, batch))
+            if time.perf_counter() - t0 >= budget_s:
+                break
+    dt = time.perf_counter() - t0
+    gbs = done_rows * wl.row_words * 4 / dt / 1e9
+    return gbs, done_rows, dt
+
+
+# ---------------------------------------------------------------- our arm --
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+
+    from trellis_quantized_weight_gb300 import binding, build
+    build.build()
+    lib = binding.load()
+
+    x, codes, scales = wl.generate()
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    n_rot = max(2, math.ceil(2 * l2 / wl.code_bytes) + 1)
+    dx = to_dev(x, torch, "bf16")
+    dscales = to_dev(scales, torch, "bf16")
+    dcodes = [to_dev(codes, torch, "u32") for _ in range(n_rot)]
+    out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = binding.gemm_workspace_bytes(wl.M, wl.K, wl.N, wl.k)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    s_handle = stream.cuda_stream
+    torch.cuda.synchronize()
+
+    def call(i):
+        rc = lib.trellis_gemm_ws(dx.data_ptr(), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
+                                 wl.M, wl.K, wl.N, wl.k, wl.L, wl.T, out.data_ptr(),
+                                 ws.data_ptr(), ws.numel(), s_handle)
+        if rc != 0:
+            raise RuntimeError(f"trellis_gemm_ws failed: {binding.status_string(rc)}")
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i)
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            starts[i].record(stream)
+            call(args.warmup + i)
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_host = time.perf_counter() - t_host0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    ms_step = total_ms / args.steps
+    kernel_ms = statistics.mean(per_launch_ms)
+    if world > 1:
+        t = torch.tensor([ms_step, kernel_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, kernel_ms = float(t[0]), float(t[1])
+
+    # ---- end to end through the public API, host buffers in pinned memory ----
+    e2e = None
+    if not args.no_e2e:
+        from trellis_quantized_weight_gb300 import gemm as tq_gemm
+        hx = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hc = torch.from_numpy(codes.view(np.int32)).pin_memory()
+        hs = torch.from_numpy(scales.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hout = torch.empty((wl.M, wl.N), dtype=torch.bfloat16).pin_memory()
+        dx2 = torch.empty_like(dx)
+        dc2 = torch.empty_like(dcodes[0])
+        ds2 = torch.empty_like(dscales)
+        n_e2e = max(3, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            dx2.copy_(hx, non_blocking=True)
+            dc2.copy_(hc, non_blocking=True)
+            ds2.copy_(hs, non_blocking=True)
+            y = tq_gemm(dx2, dc2, ds2, wl.k)
+            hout.copy_(y, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        h2d = hx.numel() * 2 + hc.numel() * 4 + hs.numel() * 2
+        e2e = {"value": round(world * wl.code_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "us_per_call": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": hout.numel() * 2}
+
+    # ---- roofline of the fused kernel (the only kernel of the step) ----
+    peaks, peak_src = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz") or 2070.0)
+    alu_peak = props.multi_processor_count * ALU_LANES_PER_SM * sm_max * 1e6 / 1e12   # Tops/s
+    ops = wl.weights * (DECODE_OPS_PER_WEIGHT + wl.M)
+    hbm_bytes = wl.code_bytes + wl.M * wl.K * 2 + wl.M * wl.N * 2
+    t_kernel = kernel_ms * 1e-3
+    alu_achieved = ops / t_kernel / 1e12
+    hbm_achieved = hbm_bytes / t_kernel / 1e9
+    t_roof_alu = ops / (alu_peak * 1e12)
+    t_roof_hbm = hbm_bytes / (float(peaks["hbm_gbs"]) * 1e9)
+    bound = "alu" if t_roof_alu >= t_roof_hbm else "hbm"
+    roof = {"bound": bound,
+            "achieved": round(alu_achieved if bound == "alu" else hbm_achieved, 3),
+            "peak": round(alu_peak if bound == "alu" else float(peaks["hbm_gbs"]), 3),
+            "unit": "Tops/s" if bound == "alu" else "GB/s",
+            "frac": round((alu_achieved / alu_peak) if bound == "alu" else
+                          (hbm_achieved / float(peaks["hbm_gbs"])), 4),
+            "traffic": profiled_traffic("gemm_smallm", wl.name),
+            "peak_source": (f"{peak_src}: {props.multi_processor_count} SMs x {ALU_LANES_PER_SM} lanes x "
+                            f"{sm_max:.0f} MHz" if bound == "alu" else f"{peak_src} hbm_gbs"),
+            "ops_per_launch": ops, "algorithmic_bytes_per_launch": hbm_bytes,
+            "hbm_GBps": round(hbm_achieved, 1),
+            "hbm_frac": round(hbm_achieved / float(peaks["hbm_gbs"]), 4),
+            "roofline_us": round(max(t_roof_alu, t_roof_hbm) * 1e6, 2),
+            "kernel_us": round(kernel_ms * 1e3, 2)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        gbs, rows, dt = oracle_throughput(wl, x, codes, scales, args.cpu_budget, threads)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} rows x K={wl.K} of {wl.name} (decode + product), {dt:.1f} s wall"}
+
+    value = world * wl.code_bytes / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "k": wl.k, "L": wl.L,
+                   "T": wl.T, "parallelism": f"replicas{world}",
+                   "l2": f"rotating {n_rot} code copies ({n_rot * wl.code_bytes / 1e6:.0f} MB > 2x L2)"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+        "clocks": clocks, "host_wall_s": round(t_host, 3),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------- reference arm --
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    x, codes, scales = wl.generate()
+    threads = os.cpu_count() or 1
+    # size each step so that warm-up + steps take about args.ref_budget seconds
+    per_step = max(0.002, args.ref_budget / max(1, args.steps + args.warmup))
+    import oracle
+    o = oracle.get()
+    t0 = time.perf_counter()
+    w = o.decode(codes, scales, wl.K, wl.N, wl.k, rows=(0, 8))
+    o.gemm_dense(x, w)
+    per_row = (time.perf_counter() - t0) / 8
+    rows = max(1, min(wl.N, int(per_step * threads / per_row)))
+
+    def step(i):
+        n0 = (i * rows) % wl.N
+        n1 = min(wl.N, n0 + rows)
+        edges = np.linspace(n0, n1, threads + 1).astype(int)
+        parts = [(int(a), int(b)) for a, b in zip(edges[:-1], edges[1:]) if b > a]
+
+        def work(r):
+            ww = o.decode(codes, scales, wl.K, wl.N, wl.k, rows=r)
+            o.gemm_dense(x, ww)
+        list(ex.map(work, parts))
+        return n1 - n0
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        for i in range(args.warmup):
+            step(i)
+        t0 = time.perf_counter()
+        done = sum(step(args.warmup + i) for i in range(args.steps))
+        dt = time.perf_counter() - t0
+    gbs = done * wl.row_words * 4 / dt / 1e9
+    ms_step = dt / args.steps * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "k": wl.k, "L": wl.L, "T": wl.T,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} rows x K={wl.K} per step (decode + product)"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds for the reference arm's timed run")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from trellis_quantized_weight_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

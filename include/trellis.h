@@ -1,0 +1,150 @@
+/*
+ * trellis.h — C ABI of the GB300 packed-Trellis decode and decode-and-multiply
+ * library (libtrellis_gb300.so).
+ *
+ * The operation is the one computed by the `mlx_bun_trellis_wide_prefill`
+ * Metal kernel on the page "mlx-bun 0.2.0 -> 0.4.0"
+ * (package/src/model/trellis-wide-prefill.ts, kernel body and the
+ * `wideTrellisPrefill` wrapper), and the dense "expand" decode named by
+ * `expandTrellis` on the page "mlx-bun 0.4.0 -> 0.5.0"
+ * (package/src/model/trellis-linear.ts).
+ *
+ * Data layout (all row-major, contiguous, caller-owned DEVICE memory):
+ *   codes  uint32 [N, K*k/32]  Each row of K weights is cut into blocks of T
+ *                              weights; a block is T*k/32 words whose bits,
+ *                              lsb first, form one bit-string.  Weight t of a
+ *                              block reads the L-bit window starting at bit
+ *                              (T-1-t)*k of that bit-string, wrapping from the
+ *                              block's last word to its word 0.
+ *   scales bf16   [N]          one scale per output row.
+ *   x      bf16   [M, K]       activations.
+ *   out    bf16   [M, N] (trellis_gemm) or [N, K] (trellis_decode).
+ * bf16 values travel as their 16-bit patterns (uint16_t).
+ *
+ * Per weight: win -> z = win*34038481 + 76625530 (mod 2^32) -> code = (sum of
+ * the bytes of z) - 510 -> value = code / 147.800537109375 (fp32, correctly
+ * rounded) -> w = bf16_rne(value * scale).  The product accumulates
+ * float(w)*float(x) in fp32 and rounds each output once to bf16 (nearest even).
+ *
+ * Accepted geometry: k in {2, 3, 4}, L == 12, T == 256, K a positive multiple
+ * of T, N >= 1, and for trellis_gemm 1 <= M <= 16.  Anything else returns
+ * TRELLIS_ERR_UNSUPPORTED or TRELLIS_ERR_SHAPE before any launch.
+ *
+ * Every call is asynchronous on `stream` (0 = the legacy default stream): it
+ * validates its arguments on the host, enqueues its kernels and returns
+ * without synchronising.  Outputs are defined once the stream has been
+ * synchronised.  A non-zero return means nothing was enqueued, except
+ * TRELLIS_ERR_CUDA, which reports the CUDA error raised by the launch itself.
+ * There is no CPU fallback.
+ */
+#ifndef TRELLIS_GB300_H
+#define TRELLIS_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle, declared the way the runtime declares it,
+ * so that this header does not need the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *cudaStream_t;
+
+#define TRELLIS_ABI_VERSION 1
+
+typedef enum trellis_status {
+    TRELLIS_OK = 0,
+    TRELLIS_ERR_NULL = -1,        /* a required pointer is NULL                        */
+    TRELLIS_ERR_SHAPE = -2,       /* sizes inconsistent or out of range (K % T != 0)   */
+    TRELLIS_ERR_UNSUPPORTED = -3, /* k, L, T or M outside the accepted set             */
+    TRELLIS_ERR_ALIGN = -4,       /* a pointer misses its required alignment           */
+    TRELLIS_ERR_CUDA = -5,        /* the CUDA runtime reported an error                */
+    TRELLIS_ERR_TIMEOUT = -6,     /* a bounded device-side wait gave up                */
+    TRELLIS_ERR_WORKSPACE = -7    /* workspace missing or smaller than required        */
+} trellis_status;
+
+/* ABI version compiled into the library (TRELLIS_ABI_VERSION). */
+int trellis_abi_version(void);
+
+/* Human-readable name of a status code; never NULL, static storage. */
+const char *trellis_status_string(int status);
+
+/*
+ * trellis_decode — expand packed codes into the dense bf16 weight matrix
+ * ("expand" mode of trellis-linear.ts on page "mlx-bun 0.4.0 -> 0.5.0"; the
+ * arithmetic is the weight decode of the wide-prefill kernel body on page
+ * "mlx-bun 0.2.0 -> 0.4.0").
+ *
+ *   codes   device, uint32 [N, K*k/32], 16-byte aligned.
+ *   scales  device, bf16 [N], 2-byte aligned.
+ *   out_bf16 device, bf16 [N, K], 16-byte aligned; fully overwritten.
+ *   out[n, b*T + t] = bf16_rne(value(window_t(block b of row n)) * scales[n]).
+ *
+ * The result is bit-exact: every weight equals the definition above.
+ * Errors: NULL pointer -> TRELLIS_ERR_NULL; misalignment -> TRELLIS_ERR_ALIGN;
+ * K <= 0, N <= 0, K % T != 0 or N*K too large -> TRELLIS_ERR_SHAPE;
+ * k, L or T outside the accepted set -> TRELLIS_ERR_UNSUPPORTED.
+ */
+int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, int k, int L,
+                   int T, uint16_t *out_bf16, cudaStream_t stream);
+
+/*
+ * trellis_gemm — fused decode-and-multiply out[m, n] = sum_k w[n, k] * x[m, k]
+ * (the wide-prefill kernel of trellis-wide-prefill.ts, page "mlx-bun 0.2.0 ->
+ * 0.4.0": each decoded weight row is shared by all M activation rows, partial
+ * sums are fp32, each output is rounded once to bf16).
+ *
+ *   x       device, bf16 [M, K], 16-byte aligned (the page's wrapper also
+ *           requires an aligned, row-contiguous x).
+ *   codes   device, uint32 [N, K*k/32], 16-byte aligned.
+ *   scales  device, bf16 [N].
+ *   out     device, bf16 [M, N]; fully overwritten.
+ *   1 <= M <= 16.
+ *
+ * The summation order is fixed by the launch geometry, so repeated calls on
+ * the same device give identical bits.  The kernel balances work across all
+ * SMs by splitting rows' K-ranges across CTAs; the split partial sums go
+ * through a workspace.  trellis_gemm uses a workspace owned by the library:
+ * the first call on each device allocates it (cudaMalloc, then zero-filled),
+ * later calls reuse it, so that first call must not happen during stream
+ * capture, and calls that use it must not overlap on the GPU (use
+ * trellis_gemm_ws with separate workspaces for concurrent streams).
+ * Errors: as trellis_decode, plus M outside 1..16 -> TRELLIS_ERR_UNSUPPORTED.
+ */
+int trellis_gemm(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M, int K,
+                 int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
+
+/*
+ * trellis_gemm_workspace_size — bytes of workspace trellis_gemm_ws needs for
+ * this geometry on the CURRENT device (it depends on the SM count).
+ * Writes the size to *bytes (may be 0).  Same validation as trellis_gemm.
+ */
+int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t *bytes);
+
+/*
+ * trellis_gemm_ws — trellis_gemm with a caller-owned workspace.
+ *
+ *   workspace        device, 256-byte aligned, at least the size reported by
+ *                    trellis_gemm_workspace_size; may be NULL only when that
+ *                    size is 0.
+ *   workspace_bytes  its size in bytes.
+ *
+ * The workspace must be zero-filled before its first use; every call leaves
+ * it zero-filled again (its tile counters reset themselves), so it can be
+ * reused without clearing.  Two calls that may overlap on the GPU must not
+ * share a workspace.  A workspace sized for one geometry serves any geometry
+ * whose reported size is not larger.
+ * Errors: as trellis_gemm, plus TRELLIS_ERR_WORKSPACE when the workspace is
+ * NULL or too small, TRELLIS_ERR_ALIGN when it is misaligned.
+ */
+int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
+                    int K, int N, int k, int L, int T, uint16_t *out, void *workspace,
+                    size_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRELLIS_GB300_H */

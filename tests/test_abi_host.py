@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads, exports every declared symbol and rejects bad
+arguments on the host (no GPU needed: validation runs before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from trellis_quantized_weight_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "trellis.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(trellis_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"trellis_decode", "trellis_gemm", "trellis_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_signatures_cover_header(lib):
+    from trellis_quantized_weight_gb300 import binding
+    assert set(declared_functions()) == set(binding.SIGNATURES)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.trellis_abi_version() == 1
+    for s in range(-7, 1):
+        assert lib.trellis_status_string(s).decode().startswith("TRELLIS_")
+    assert lib.trellis_status_string(123).decode() == "TRELLIS_ERR_UNKNOWN"
+
+
+FAKE = 0x10000   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("args,want", [
+    ((0, FAKE, 5120, 8, 4, 12, 256, FAKE, None), -1),          # NULL codes
+    ((FAKE, 0, 5120, 8, 4, 12, 256, FAKE, None), -1),          # NULL scales
+    ((FAKE, FAKE, 5120, 8, 4, 12, 256, 0, None), -1),          # NULL out
+    ((FAKE, FAKE, 5120, 8, 5, 12, 256, FAKE, None), -3),       # k = 5
+    ((FAKE, FAKE, 5120, 8, 1, 12, 256, FAKE, None), -3),       # k = 1
+    ((FAKE, FAKE, 5120, 8, 4, 11, 256, FAKE, None), -3),       # L = 11
+    ((FAKE, FAKE, 5120, 8, 4, 12, 128, FAKE, None), -3),       # T = 128
+    ((FAKE, FAKE, 5000, 8, 4, 12, 256, FAKE, None), -2),       # K % T != 0
+    ((FAKE, FAKE, 0, 8, 4, 12, 256, FAKE, None), -2),          # K = 0
+    ((FAKE, FAKE, 5120, 0, 4, 12, 256, FAKE, None), -2),       # N = 0
+    ((FAKE, FAKE, 5120, -3, 4, 12, 256, FAKE, None), -2),      # N < 0
+    ((FAKE + 4, FAKE, 5120, 8, 4, 12, 256, FAKE, None), -4),   # codes not 16-B aligned
+    ((FAKE, FAKE + 1, 5120, 8, 4, 12, 256, FAKE, None), -4),   # scales odd address
+    ((FAKE, FAKE, 5120, 8, 4, 12, 256, FAKE + 8, None), -4),   # out not 16-B aligned
+    ((FAKE, FAKE, 2 ** 30, 2 ** 20, 4, 12, 256, FAKE, None), -2),   # too many (row, block) items
+])
+def test_decode_rejects(lib, args, want):
+    assert lib.trellis_decode(*args) == want
+
+
+@pytest.mark.parametrize("M,K,N,k,L,T,want", [
+    (0, 5120, 64, 4, 12, 256, -3), (17, 5120, 64, 4, 12, 256, -3), (64, 5120, 64, 4, 12, 256, -3),
+    (5, 5120, 64, 6, 12, 256, -3), (5, 5000, 64, 4, 12, 256, -2), (5, 5120, 0, 4, 12, 256, -2),
+])
+def test_gemm_rejects(lib, M, K, N, k, L, T, want):
+    assert lib.trellis_gemm(FAKE, FAKE, FAKE, M, K, N, k, L, T, FAKE, None) == want
+    assert lib.trellis_gemm_ws(FAKE, FAKE, FAKE, M, K, N, k, L, T, FAKE, FAKE, 1 << 20, None) == want
+    n = ctypes.c_size_t(0)
+    assert lib.trellis_gemm_workspace_size(M, K, N, k, L, T, ctypes.byref(n)) == want
+
+
+def test_gemm_rejects_pointers(lib):
+    assert lib.trellis_gemm(0, FAKE, FAKE, 5, 5120, 64, 4, 12, 256, FAKE, None) == -1
+    assert lib.trellis_gemm(FAKE, FAKE, FAKE, 5, 5120, 64, 4, 12, 256, 0, None) == -1
+    assert lib.trellis_gemm(FAKE + 2, FAKE, FAKE, 5, 5120, 64, 4, 12, 256, FAKE, None) == -4
+    assert lib.trellis_gemm(FAKE, FAKE + 4, FAKE, 5, 5120, 64, 4, 12, 256, FAKE, None) == -4
+    assert lib.trellis_gemm(FAKE, FAKE, FAKE, 5, 5120, 64, 4, 12, 256, FAKE + 1, None) == -4
+    assert lib.trellis_gemm_workspace_size(5, 5120, 64, 4, 12, 256, None) == -1
+
+
+def test_product_path_has_no_oracle_import():
+    """The package never imports the oracle (the oracle is test infrastructure)."""
+    pkg = os.path.join(ROOT, "trellis_quantized_weight_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), f
+                assert "trellis_oracle" not in src and "liboracle" not in src, f

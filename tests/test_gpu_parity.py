@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Decode must match bit for bit.  The product must stay within
+max(2 bf16 ulp, 1e-4 * sum_k |w_k x_k|) of the oracle's exactly summed fp32
+result, element by element.  Shapes span several tiles, ragged tails, single
+blocks, splits of one row's K-range over many CTAs and CTAs that own whole
+tile-groups, plus the full-size quantised-linear workloads.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from helpers import (assert_gemm_close, bf16_to_f32, dev_bf16, dev_codes, host_bits,
+                     oracle_decode_par, oracle_gemm_par)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tq():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from trellis_quantized_weight_gb300 import build
+    build.build()
+    import trellis_quantized_weight_gb300 as tq
+    tq.load()
+    return tq
+
+
+def _inputs(M, K, N, k, seed, sigma=1.0):
+    from trellis_quantized_weight_gb300 import synth
+    return synth.small(M, K, N, k, seed, sigma).generate()
+
+
+# ------------------------------------------------------------------ decode --
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("N,K", [(1, 256), (3, 256), (33, 512), (1000, 1024), (77, 256 * 13)])
+def test_decode_bitexact(tq, oracle_lib, k, N, K):
+    _, codes, scales = _inputs(1, K, N, k, seed=1000 * k + N + K)
+    got = host_bits(tq.decode(dev_codes(codes), dev_bf16(scales), K, k))
+    want = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_decode_crafted_blocks(tq, oracle_lib, k):
+    """Blocks that light up the wrap from the last word to word 0 and every word edge."""
+    T, wpb = 256, 256 * k // 32
+    rows = []
+    for bit in list(range(0, 32)) + [T * k - 1 - i for i in range(32)] + [32 * i + 31 for i in range(wpb)]:
+        r = np.zeros(wpb, np.uint32)
+        r[bit // 32] |= np.uint32(1 << (bit % 32))
+        rows.append(r)
+    rows.append(np.full(wpb, 0xFFFFFFFF, np.uint32))
+    rows.append(np.zeros(wpb, np.uint32))
+    codes = np.stack(rows)
+    N = codes.shape[0]
+    scales = np.full(N, 0x3F80, np.uint16)       # 1.0: weights are bf16(value) directly
+    got = host_bits(tq.decode(dev_codes(codes), dev_bf16(scales), T, k))
+    want = oracle_lib.decode(codes, scales, T, N, k)
+    assert np.array_equal(got, want)
+    assert np.all(got[-2] == 0x3FA3) and np.all(got[-1] == 0xBFA0)   # hand-worked values
+
+
+# -------------------------------------------------------------------- gemm --
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 12, 15, 16])
+def test_gemm_small(tq, oracle_lib, M, k):
+    N, K = 1000, 1024
+    x, codes, scales = _inputs(M, K, N, k, seed=77 * M + k)
+    got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), k))
+    w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+    ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+    assert_gemm_close(got, ref, refabs, f"M={M} k={k}")
+
+
+@pytest.mark.parametrize("M,K,N,k", [
+    (1, 256, 1, 2), (3, 256, 5, 3), (5, 512, 33, 4), (16, 256 * 7, 129, 2),
+    (8, 256, 40000, 3),          # many tile-groups, K of one block
+    (2, 256, 200000, 4),         # CTAs owning whole tile-groups (no split)
+    (9, 256, 90000, 2),          # same with the 8-warp shape
+    (1, 256 * 70, 64, 4),        # one tile-group split over every CTA
+])
+def test_gemm_shapes(tq, oracle_lib, M, K, N, k):
+    x, codes, scales = _inputs(M, K, N, k, seed=M * 131 + K + N + k)
+    got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), k))
+    w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+    ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+    assert_gemm_close(got, ref, refabs, f"M={M} K={K} N={N} k={k}")
+
+
+def test_gemm_one_hot_is_exact(tq, oracle_lib):
+    """x = e_j picks column j of the decoded weights, bit for bit."""
+    N, K, k = 700, 1280, 3
+    _, codes, scales = _inputs(1, K, N, k, seed=5)
+    w = oracle_lib.decode(codes, scales, K, N, k)
+    for j in (0, 255, 256, 777, K - 1):
+        e = np.zeros((1, K), np.uint16)
+        e[0, j] = 0x3F80
+        got = host_bits(tq.gemm(dev_bf16(e), dev_codes(codes), dev_bf16(scales), k))
+        assert np.array_equal(got[0], w[:, j])
+
+
+def test_gemm_deterministic(tq):
+    x, codes, scales = _inputs(15, 5120, 3000, 4, seed=9)
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    a = host_bits(tq.gemm(dx, dc, ds, 4))
+    b = host_bits(tq.gemm(dx, dc, ds, 4))
+    assert np.array_equal(a, b)
+
+
+def test_gemm_library_workspace_matches(tq):
+    """trellis_gemm (library-owned workspace) equals trellis_gemm_ws (caller's)."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    M, K, N, k = 5, 2048, 2000, 2
+    x, codes, scales = _inputs(M, K, N, k, seed=12)
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    a = host_bits(tq.gemm(dx, dc, ds, k))
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    rc = binding.abi_gemm(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256,
+                          out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(a, host_bits(out))
+
+
+def test_gemm_workspace_errors(tq):
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    M, K, N, k = 4, 1024, 5000, 4
+    x, codes, scales = _inputs(M, K, N, k, seed=3)
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    need = binding.gemm_workspace_bytes(M, K, N, k)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    args = (dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256, out.data_ptr())
+    assert binding.abi_gemm_ws(*args, ws.data_ptr(), need - 1, s) == -7
+    assert binding.abi_gemm_ws(*args, 0, need, s) == -7
+    assert binding.abi_gemm_ws(*args, ws.data_ptr() + 4, need - 4, s) in (-4, -7)
+    assert binding.abi_gemm_ws(*args, ws.data_ptr(), need, s) == 0
+    # misaligned x (2-byte offset into a bf16 buffer)
+    big = torch.zeros(M * K + 8, dtype=torch.bfloat16, device="cuda")
+    assert binding.abi_gemm_ws(big.data_ptr() + 2, *args[1:], ws.data_ptr(), need, s) == -4
+    torch.cuda.synchronize()
+
+
+# ----------------------------------------------- full-size quantised-linear --
+WORKLOADS_SMALL_M = ["gemm_m5_k5120_n17408_k2", "gemm_m8_k5120_n17408_k3",
+                     "gemm_m15_k5120_n17408_k4", "gemv_m1_k17408_n5120_k4"]
+ALL_WORKLOADS = WORKLOADS_SMALL_M + ["prefill_m64_k5120_n17408_k4"]
+
+
+@pytest.fixture(scope="module")
+def full_inputs():
+    from trellis_quantized_weight_gb300 import synth
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            cache.clear()
+            wl = synth.WORKLOADS[name]
+            cache[name] = (wl, *wl.generate())
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("name", ALL_WORKLOADS)
+def test_full_decode_bitexact(tq, oracle_lib, full_inputs, name):
+    wl, x, codes, scales = full_inputs(name)
+    got = host_bits(tq.decode(dev_codes(codes), dev_bf16(scales), wl.K, wl.k))
+    want = oracle_decode_par(oracle_lib, codes, scales, wl.K, wl.N, wl.k)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("name", WORKLOADS_SMALL_M)
+def test_full_gemm(tq, oracle_lib, full_inputs, name):
+    wl, x, codes, scales = full_inputs(name)
+    got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), wl.k))
+    w = oracle_decode_par(oracle_lib, codes, scales, wl.K, wl.N, wl.k)
+    ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+    assert_gemm_close(got, ref, refabs, name)

@@ -1,0 +1,36 @@
+// Host dispatch of the small-M fused decode-and-multiply (plan, workspace size,
+// bit-width switch).  The kernels live in gemm_smallm_k{2,3,4}.cu.
+#include "gemm_smallm_kernel.cuh"
+
+namespace trellis {
+
+template <int MM>
+static size_t ws_bytes_for(int K, int N, int k, const DeviceInfo& dev) {
+    return smallm_workspace_bytes<MM>(plan_smallm<MM>(K, N, k, dev));
+}
+
+size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo& dev) {
+    switch (M) {
+#define TRELLIS_CASE(MV) \
+    case MV: return ws_bytes_for<MV>(K, N, k, dev);
+        TRELLIS_CASE(1) TRELLIS_CASE(2) TRELLIS_CASE(3) TRELLIS_CASE(4)
+        TRELLIS_CASE(5) TRELLIS_CASE(6) TRELLIS_CASE(7) TRELLIS_CASE(8)
+        TRELLIS_CASE(9) TRELLIS_CASE(10) TRELLIS_CASE(11) TRELLIS_CASE(12)
+        TRELLIS_CASE(13) TRELLIS_CASE(14) TRELLIS_CASE(15) TRELLIS_CASE(16)
+#undef TRELLIS_CASE
+        default: return 0;
+    }
+}
+
+int launch_gemm_smallm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M,
+                       int K, int N, int k, uint16_t* out, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream, const DeviceInfo& dev) {
+    switch (k) {
+        case 2: return launch_smallm_k<2>(M, x, codes, scales, K, N, out, workspace, workspace_bytes, stream, dev);
+        case 3: return launch_smallm_k<3>(M, x, codes, scales, K, N, out, workspace, workspace_bytes, stream, dev);
+        case 4: return launch_smallm_k<4>(M, x, codes, scales, K, N, out, workspace, workspace_bytes, stream, dev);
+        default: return -3;
+    }
+}
+
+}  // namespace trellis

@@ -1,0 +1,32 @@
+// Internal launch interface between the C ABI (trellis_abi.cu) and the kernel
+// translation units.  Arguments reaching these functions are already validated.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace trellis {
+
+// The geometry the kernels are compiled for (the envelope of the page's
+// wrapper: 12-bit windows, 256-weight blocks).
+constexpr int kL_abi = 12;
+constexpr int kT_abi = 256;
+
+struct DeviceInfo {
+    int device = 0;
+    int num_sms = 0;
+    int max_smem_optin = 0;   // bytes of dynamic shared memory a CTA may opt into
+};
+
+// Dense decode of all N rows into out [N, K].  Returns 0 or a trellis_status.
+int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
+                  uint16_t* out, cudaStream_t stream, const DeviceInfo& dev);
+
+// Fused decode-and-multiply for 1 <= M <= 16 (CUDA cores).
+size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo& dev);
+int launch_gemm_smallm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M,
+                       int K, int N, int k, uint16_t* out, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream, const DeviceInfo& dev);
+
+}  // namespace trellis

@@ -1,0 +1,179 @@
+// The C ABI (include/trellis.h): argument validation on the host, then one
+// kernel launch on the caller's stream.  No host synchronisation, no CPU
+// fallback.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "trellis.h"
+
+namespace {
+
+using trellis::DeviceInfo;
+
+constexpr int kMaxDevices = 64;
+
+int device_info(DeviceInfo& out) {
+    static std::mutex mu;
+    static DeviceInfo cache[kMaxDevices];
+    static bool have[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TRELLIS_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        DeviceInfo d;
+        d.device = dev;
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return TRELLIS_ERR_CUDA;
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    out = cache[dev];
+    return TRELLIS_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Checks shared by every entry point (geometry envelope of the page's wrapper:
+// k in {2,3,4}, L = 12, T = 256; K a multiple of T; no fixed K or N).
+int check_geometry(int K, int N, int k, int L, int T) {
+    if (k != 2 && k != 3 && k != 4) return TRELLIS_ERR_UNSUPPORTED;
+    if (L != trellis::kL_abi || T != trellis::kT_abi) return TRELLIS_ERR_UNSUPPORTED;
+    if (K <= 0 || N <= 0 || K % T != 0) return TRELLIS_ERR_SHAPE;
+    // item (row, block) indices and weight offsets must fit the kernels' integer types
+    const long long items = static_cast<long long>(N) * (K / T);
+    if (items >= (1ll << 31)) return TRELLIS_ERR_SHAPE;
+    return TRELLIS_OK;
+}
+
+int check_codes(const uint32_t* codes, const uint16_t* scales) {
+    if (codes == nullptr || scales == nullptr) return TRELLIS_ERR_NULL;
+    if (!aligned(codes, 16) || !aligned(scales, 2)) return TRELLIS_ERR_ALIGN;
+    return TRELLIS_OK;
+}
+
+int check_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
+               int k, int L, int T, const uint16_t* out) {
+    if (x == nullptr || out == nullptr) return TRELLIS_ERR_NULL;
+    int rc = check_codes(codes, scales);
+    if (rc != TRELLIS_OK) return rc;
+    rc = check_geometry(K, N, k, L, T);
+    if (rc != TRELLIS_OK) return rc;
+    if (M < 1 || M > 16) return TRELLIS_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(out, 2)) return TRELLIS_ERR_ALIGN;
+    return TRELLIS_OK;
+}
+
+// Library-owned workspace of trellis_gemm, one per device, grown on demand.
+struct OwnedWorkspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+
+int owned_workspace(const DeviceInfo& dev, size_t need, void** ptr) {
+    static std::mutex mu;
+    static OwnedWorkspace ws[kMaxDevices];
+    std::lock_guard<std::mutex> lock(mu);
+    OwnedWorkspace& w = ws[dev.device];
+    if (w.bytes < need) {
+        // growing: wait for work that may still use the old buffer
+        if (w.ptr != nullptr) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return TRELLIS_ERR_CUDA;
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        void* p = nullptr;
+        if (cudaMalloc(&p, need) != cudaSuccess) return TRELLIS_ERR_CUDA;
+        if (cudaMemset(p, 0, need) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaFree(p);
+            return TRELLIS_ERR_CUDA;
+        }
+        w.ptr = p;
+        w.bytes = need;
+    }
+    *ptr = w.ptr;
+    return TRELLIS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int trellis_abi_version(void) { return TRELLIS_ABI_VERSION; }
+
+const char* trellis_status_string(int status) {
+    switch (status) {
+        case TRELLIS_OK: return "TRELLIS_OK";
+        case TRELLIS_ERR_NULL: return "TRELLIS_ERR_NULL: a required pointer is NULL";
+        case TRELLIS_ERR_SHAPE: return "TRELLIS_ERR_SHAPE: sizes inconsistent or out of range";
+        case TRELLIS_ERR_UNSUPPORTED: return "TRELLIS_ERR_UNSUPPORTED: k, L, T or M outside the accepted set";
+        case TRELLIS_ERR_ALIGN: return "TRELLIS_ERR_ALIGN: a pointer misses its required alignment";
+        case TRELLIS_ERR_CUDA: return "TRELLIS_ERR_CUDA: the CUDA runtime reported an error";
+        case TRELLIS_ERR_TIMEOUT: return "TRELLIS_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case TRELLIS_ERR_WORKSPACE: return "TRELLIS_ERR_WORKSPACE: workspace missing or too small";
+        default: return "TRELLIS_ERR_UNKNOWN";
+    }
+}
+
+int trellis_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k, int L, int T,
+                   uint16_t* out_bf16, cudaStream_t stream) {
+    int rc = check_codes(codes, scales);
+    if (rc != TRELLIS_OK) return rc;
+    if (out_bf16 == nullptr) return TRELLIS_ERR_NULL;
+    rc = check_geometry(K, N, k, L, T);
+    if (rc != TRELLIS_OK) return rc;
+    if (!aligned(out_bf16, 16)) return TRELLIS_ERR_ALIGN;
+    DeviceInfo dev;
+    rc = device_info(dev);
+    if (rc != TRELLIS_OK) return rc;
+    return trellis::launch_decode(codes, scales, K, N, k, out_bf16, stream, dev);
+}
+
+int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t* bytes) {
+    if (bytes == nullptr) return TRELLIS_ERR_NULL;
+    int rc = check_geometry(K, N, k, L, T);
+    if (rc != TRELLIS_OK) return rc;
+    if (M < 1 || M > 16) return TRELLIS_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    rc = device_info(dev);
+    if (rc != TRELLIS_OK) return rc;
+    *bytes = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
+    return TRELLIS_OK;
+}
+
+int trellis_gemm_ws(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K,
+                    int N, int k, int L, int T, uint16_t* out, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream) {
+    int rc = check_gemm(x, codes, scales, M, K, N, k, L, T, out);
+    if (rc != TRELLIS_OK) return rc;
+    DeviceInfo dev;
+    rc = device_info(dev);
+    if (rc != TRELLIS_OK) return rc;
+    const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return TRELLIS_ERR_WORKSPACE;
+    if (workspace != nullptr && !aligned(workspace, 256)) return TRELLIS_ERR_ALIGN;
+    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, workspace, workspace_bytes,
+                                       stream, dev);
+}
+
+int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
+                 int k, int L, int T, uint16_t* out, cudaStream_t stream) {
+    int rc = check_gemm(x, codes, scales, M, K, N, k, L, T, out);
+    if (rc != TRELLIS_OK) return rc;
+    DeviceInfo dev;
+    rc = device_info(dev);
+    if (rc != TRELLIS_OK) return rc;
+    const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
+    void* ws = nullptr;
+    if (need > 0) {
+        rc = owned_workspace(dev, need, &ws);
+        if (rc != TRELLIS_OK) return rc;
+    }
+    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, ws, need, stream, dev);
+}
+
+}  // extern "C"

@@ -1,0 +1,124 @@
+// Device-side building blocks of the packed-Trellis decode (sm_103a).
+//
+// The per-weight arithmetic follows the wide-prefill Metal kernel on the page
+// "mlx-bun 0.2.0 -> 0.4.0" (package/src/model/trellis-wide-prefill.ts): an
+// L-bit window of the block's bit-string, the multiply-add hash, the sum of the
+// hash's four bytes minus 510, the residual-corrected fp32 quotient by
+// 147.800537109375, the per-row scale and a round to bf16.
+//
+// Work is organised in "groups" of 32 consecutive weights of one block
+// (T = 256 weights, so 8 groups per block).  Group g holds weights
+// t = 32g .. 32g+31, which start at bits (T-1-t)*k; those are exactly the k
+// words (8-1-g)*k .. (8-g)*k-1 of the block, plus the window tails that spill
+// into the next word: word (8-g)*k, which for g = 0 wraps to word 0 of the
+// same block.  Inside a group the bit offset of weight j is the compile-time
+// constant (31-j)*k, so every shift below folds to an immediate.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace trellis {
+
+constexpr int kT = 256;                 // weights per block
+constexpr int kL = 12;                  // window bits
+constexpr int kGroupsPerBlock = kT / 32;
+
+constexpr uint32_t kHashMul = 34038481u;
+constexpr uint32_t kHashAdd = 76625530u;
+constexpr float kDivisor = 147.800537109375f;
+constexpr float kRecip = 1.0f / 147.800537109375f;   // fp32 round-to-nearest of 1/c
+// dp4a(z, 0x01010101, 0x4B400000) is the bit pattern of the float
+// 1.5*2^23 + (byte sum), exactly; subtracting 1.5*2^23 + 510 leaves
+// float(code) exactly (both operands share the exponent 2^23, unit ulp).
+constexpr uint32_t kMagicBits = 0x4B400000u;
+constexpr float kMagicPlusBias = 12583422.0f;
+
+// Window of weight j (0..31) of a group, from the group's k words w[0..k-1]
+// and the lookahead word w[k].
+template <int KB>
+__device__ __forceinline__ uint32_t group_window(const uint32_t (&w)[KB + 1], int j) {
+    const int o = (31 - j) * KB;     // constant after unrolling
+    const int wi = o >> 5;
+    const int off = o & 31;
+    uint32_t win;
+    if (off + kL <= 32)
+        win = w[wi] >> off;
+    else
+        win = __funnelshift_r(w[wi], w[wi + 1], off);
+    return win & ((1u << kL) - 1u);
+}
+
+// 12-bit window -> fp32 value, bit-exact with code / 147.800537109375.
+__device__ __forceinline__ float window_value(uint32_t win) {
+    const uint32_t z = win * kHashMul + kHashAdd;
+    const float biased = __uint_as_float(__dp4a(z, 0x01010101u, kMagicBits));
+    const float code = __fsub_rn(biased, kMagicPlusBias);
+    const float approx = __fmul_rn(code, kRecip);
+    const float residual = __fmaf_rn(-approx, kDivisor, code);
+    return __fmaf_rn(residual, kRecip, approx);
+}
+
+// bf16 round-to-nearest-even of w, returned as the fp32 with the same value
+// (the bf16 bits in the upper half, zeros below).
+__device__ __forceinline__ float round_bf16_as_f32(float w) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(w), "f"(0.0f));
+    return __uint_as_float(r);
+}
+
+// Two floats -> packed bf16x2 (lo in the low half, i.e. at the lower address).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint16_t bf16_bits_rn(float f) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// Loads the k words of group g of a block (bw = first word of the block) and
+// the lookahead word.
+template <int KB>
+__device__ __forceinline__ void load_group_words(const uint32_t* __restrict__ bw, int g,
+                                                 uint32_t (&w)[KB + 1]) {
+    const uint32_t* p = bw + (kGroupsPerBlock - 1 - g) * KB;
+    if constexpr (KB == 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (KB == 2) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+        w[0] = v.x; w[1] = v.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < KB; ++i) w[i] = __ldg(p + i);
+    }
+    const int la = ((kGroupsPerBlock - g) * KB) % (kGroupsPerBlock * KB);
+    w[KB] = __ldg(bw + la);
+}
+
+// Exact unsigned 32-bit division by a runtime constant d >= 1
+// (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994): q = (mulhi(n, m) + n) >> l.
+struct FastDiv {
+    uint32_t d, m, l;
+    __host__ __device__ FastDiv() : d(1), m(0), l(0) {}
+    __host__ explicit FastDiv(uint32_t divisor) : d(divisor) {
+        l = 0;
+        while ((1ull << l) < divisor) ++l;
+        m = static_cast<uint32_t>((((1ull << l) - divisor) << 32) / divisor + 1);
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(n, m)) + n) >> l);
+    }
+};
+
+}  // namespace trellis
