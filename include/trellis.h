@@ -119,7 +119,7 @@ int trellis_gemm(const uint16_t *x, const uint32_t *codes, const uint16_t *scale
 /*
  * trellis_gemm_workspace_size — bytes of workspace trellis_gemm_ws needs for
  * this geometry on the CURRENT device (it depends on the SM count).
- * Writes the size to *bytes (may be 0).  Same validation as trellis_gemm.
+ * Writes the size to *bytes.  Same validation as trellis_gemm.
  */
 int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t *bytes);
 
@@ -127,13 +127,15 @@ int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t
  * trellis_gemm_ws — trellis_gemm with a caller-owned workspace.
  *
  *   workspace        device, 256-byte aligned, at least the size reported by
- *                    trellis_gemm_workspace_size; may be NULL only when that
- *                    size is 0.
+ *                    trellis_gemm_workspace_size.
  *   workspace_bytes  its size in bytes.
  *
- * The workspace must be zero-filled before its first use; every call leaves
- * it zero-filled again (its tile counters reset themselves), so it can be
- * reused without clearing.  Two calls that may overlap on the GPU must not
+ * The workspace must be zero-filled before its first use.  Its first
+ * 1 MiB holds per-tile counters that every completed call leaves at zero; the
+ * rest holds partial sums that need no clearing, so the workspace can be
+ * reused, for any geometry that fits it, without clearing.  Geometries with
+ * more than 2^18 row tiles (tiles are 64 rows) are rejected with
+ * TRELLIS_ERR_SHAPE.  Two calls that may overlap on the GPU must not
  * share a workspace.  A workspace sized for one geometry serves any geometry
  * whose reported size is not larger.
  * Errors: as trellis_gemm, plus TRELLIS_ERR_WORKSPACE when the workspace is

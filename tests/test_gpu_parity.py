@@ -126,6 +126,29 @@ def test_gemm_library_workspace_matches(tq):
     assert np.array_equal(a, host_bits(out))
 
 
+def test_gemm_workspace_reuse_across_geometries(tq, oracle_lib):
+    """One workspace serves a sequence of geometries without clearing: the tile
+    counters sit at a fixed place and every call leaves them at zero."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    cases = [(8, 256, 40000, 3), (2, 256, 100000, 4), (1, 256 * 70, 64, 4), (15, 1024, 3000, 2),
+             (8, 256, 40000, 3)]
+    need = max(binding.gemm_workspace_bytes(M, K, N, k) for M, K, N, k in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    for i, (M, K, N, k) in enumerate(cases):
+        x, codes, scales = _inputs(M, K, N, k, seed=900 + i)
+        dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        assert binding.abi_gemm_ws(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256,
+                                   out.data_ptr(), ws.data_ptr(), need, s) == 0
+        torch.cuda.synchronize()
+        w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+        ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+        assert_gemm_close(host_bits(out), ref, refabs, f"case {i}")
+        assert int(ws[: 1 << 20].count_nonzero()) == 0, "tile counters not left at zero"
+
+
 def test_gemm_workspace_errors(tq):
     import torch
     from trellis_quantized_weight_gb300 import binding

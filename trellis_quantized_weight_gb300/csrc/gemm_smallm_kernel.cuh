@@ -260,12 +260,23 @@ SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev) {
     return p;
 }
 
+// Workspace layout: a fixed-capacity counter region at offset 0 (the same
+// place for every geometry, so a workspace reused across geometries never
+// finds stale partial sums where it expects counters), then the partial sums.
+// Counters are left at zero by every call; partial sums need no clearing.
+constexpr size_t kCounterCapacity = size_t(1) << 18;            // tiles
+constexpr size_t kCounterBytes = kCounterCapacity * sizeof(uint32_t);
+
 template <int MM>
 size_t smallm_workspace_bytes(const SmallMPlan& p) {
     using S = SmallMShape<MM>;
-    const size_t counters = (static_cast<size_t>(p.ntg) * S::WARPS * 4 + 255) / 256 * 256;
     const size_t partials = static_cast<size_t>(p.P) * 2 * S::WARPS * MM * S::R * 32 * 4;
-    return counters + partials;
+    return kCounterBytes + partials;
+}
+
+template <int MM>
+bool smallm_fits_counters(const SmallMPlan& p) {
+    return static_cast<size_t>(p.ntg) * SmallMShape<MM>::WARPS <= kCounterCapacity;
 }
 
 template <int MM, int KB>
@@ -274,11 +285,11 @@ int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint1
                            cudaStream_t stream, const DeviceInfo& dev) {
     using S = SmallMShape<MM>;
     SmallMPlan p = plan_smallm<MM>(K, N, KB, dev);
+    if (!smallm_fits_counters<MM>(p)) return -2;
     const size_t need = smallm_workspace_bytes<MM>(p);
     if (ws_bytes < need || ws == nullptr) return -7;
-    const size_t counters = (static_cast<size_t>(p.ntg) * S::WARPS * 4 + 255) / 256 * 256;
     p.counters = static_cast<uint32_t*>(ws);
-    p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + counters);
+    p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
     const size_t smem = static_cast<size_t>(p.units_max) * S::XS_UNIT * 4;
     static bool attr_set = false;   // idempotent; a race only repeats the call
     if (!attr_set) {

@@ -142,7 +142,7 @@ int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
     *bytes = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
-    return TRELLIS_OK;
+    return *bytes == 0 ? TRELLIS_ERR_SHAPE : TRELLIS_OK;
 }
 
 int trellis_gemm_ws(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K,
@@ -154,8 +154,9 @@ int trellis_gemm_ws(const uint16_t* x, const uint32_t* codes, const uint16_t* sc
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
     const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
-    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return TRELLIS_ERR_WORKSPACE;
-    if (workspace != nullptr && !aligned(workspace, 256)) return TRELLIS_ERR_ALIGN;
+    if (need == 0) return TRELLIS_ERR_SHAPE;
+    if (workspace == nullptr || workspace_bytes < need) return TRELLIS_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return TRELLIS_ERR_ALIGN;
     return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, workspace, workspace_bytes,
                                        stream, dev);
 }
@@ -168,11 +169,10 @@ int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scale
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
     const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
+    if (need == 0) return TRELLIS_ERR_SHAPE;
     void* ws = nullptr;
-    if (need > 0) {
-        rc = owned_workspace(dev, need, &ws);
-        if (rc != TRELLIS_OK) return rc;
-    }
+    rc = owned_workspace(dev, need, &ws);
+    if (rc != TRELLIS_OK) return rc;
     return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, ws, need, stream, dev);
 }
 
