@@ -145,6 +145,29 @@ int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *sc
                     int K, int N, int k, int L, int T, uint16_t *out, void *workspace,
                     size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * trellis_gemm_noalloc — trellis_gemm for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a library convenience.
+ *
+ * Same arguments, validation, arithmetic and results as trellis_gemm, but the
+ * scratch memory of the split-K reduction comes from a fixed 16 MiB array that
+ * the library holds on every GPU that loads it, until the process exits.  It
+ * never calls cudaMalloc, cudaFree or any allocating routine, so it suits code
+ * that must not allocate: allocator or memory-pool callbacks, processes that
+ * reserve all device memory up front, runtimes that forbid allocation on the
+ * hot path.
+ *
+ * The first call on each device does a one-time set-up with that device
+ * current (it looks up the array's device address and clears its counter
+ * region, synchronising the device); make that first call before any stream
+ * capture.  Every call shares the array: calls that may overlap on the same
+ * GPU (for instance on two streams) race and must be serialised by the caller.
+ * Geometries whose scratch (as reported by trellis_gemm_workspace_size) exceeds
+ * 16 MiB are rejected with TRELLIS_ERR_WORKSPACE before any launch.
+ */
+int trellis_gemm_noalloc(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
+                         int K, int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,94 @@
+"""trellis_gemm_noalloc: the decode-and-multiply for callers that cannot allocate.
+
+Some callers may not call cudaMalloc: code running inside an allocator or a
+memory-pool callback, processes that reserve all device memory up front, or
+runtimes that forbid allocation on their hot path.  trellis_gemm_noalloc serves
+them by taking its split-K scratch from a fixed array inside the library.
+
+Each case calls it twice in a row through the C ABI (the second call finds the
+scratch exactly as the first left it) and compares both outputs with the
+existing entry point trellis_gemm_ws, within the product tolerance
+max(2 bf16 ulp, 1e-4 * sum_k |w_k x_k|).  This file is collected last and also
+passes on its own in a fresh process.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+FAKE = 0x10000   # aligned, never dereferenced: only used where validation rejects first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from trellis_quantized_weight_gb300 import binding, build
+    build.build()
+    return binding.load()
+
+
+def _dev(a, torch, bf16):
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16 if bf16 else np.int32)).cuda()
+    return t.view(torch.bfloat16) if bf16 else t
+
+
+@pytest.mark.parametrize("M,K,N,k", [
+    (8, 5120, 17408, 3),       # the headline shape
+    (15, 5120, 6000, 4),
+    (1, 17408, 5120, 4),
+    (5, 256, 40000, 2),
+])
+def test_noalloc_matches_gemm_ws(lib, M, K, N, k):
+    import torch
+    from trellis_quantized_weight_gb300 import binding, synth
+    x, codes, scales = synth.small(M, K, N, k, seed=4242 + M + k).generate()
+    dx, dc, ds = _dev(x, torch, True), _dev(codes, torch, False), _dev(scales, torch, True)
+    s = torch.cuda.current_stream().cuda_stream
+
+    need = binding.gemm_workspace_bytes(M, K, N, k)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert lib.trellis_gemm_ws(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256,
+                               ref.data_ptr(), ws.data_ptr(), need, s) == 0
+
+    # tolerance from the decoded weights: 1e-4 * sum_k |w x| and 2 bf16 ulp of the reference
+    w = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    assert lib.trellis_decode(dc.data_ptr(), ds.data_ptr(), K, N, k, 12, 256, w.data_ptr(), s) == 0
+    refabs = dx.double().abs() @ w.double().abs().T
+    reff = ref.double()
+    ulp = torch.exp2(torch.floor(torch.log2(reff.abs().clamp_min(2.0 ** -126))) - 7)
+    tol = torch.maximum(2 * ulp, 1e-4 * refabs)
+
+    for call in range(2):
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        rc = lib.trellis_gemm_noalloc(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256,
+                                      out.data_ptr(), s)
+        assert rc == 0, binding.status_string(rc)
+        torch.cuda.synchronize()
+        err = (out.double() - reff).abs()
+        assert bool(torch.all(err <= tol)), f"call {call}: max excess {float((err - tol).max())}"
+
+
+def test_noalloc_rejects_bad_arguments(lib):
+    assert lib.trellis_gemm_noalloc(0, FAKE, FAKE, 8, 5120, 64, 3, 12, 256, FAKE, None) == -1
+    assert lib.trellis_gemm_noalloc(FAKE + 2, FAKE, FAKE, 8, 5120, 64, 3, 12, 256, FAKE, None) == -4
+    assert lib.trellis_gemm_noalloc(FAKE, FAKE, FAKE, 17, 5120, 64, 3, 12, 256, FAKE, None) == -3
+    assert lib.trellis_gemm_noalloc(FAKE, FAKE, FAKE, 8, 5000, 64, 3, 12, 256, FAKE, None) == -2
+
+
+def test_noalloc_rejects_geometry_beyond_its_scratch(lib):
+    """A geometry whose scratch exceeds the fixed 16 MiB array is refused before any launch."""
+    from trellis_quantized_weight_gb300 import binding
+    limit = 16 << 20
+    found = None
+    for N in (1 << 20, 1 << 21, 1 << 22, (1 << 23) - 256, (1 << 24) - 256):
+        try:
+            if binding.gemm_workspace_bytes(16, 256, N, 4) > limit:
+                found = N
+                break
+        except binding.TrellisError:
+            break
+    if found is None:
+        pytest.skip("no accepted geometry needs more than 16 MiB of scratch on this device")
+    assert lib.trellis_gemm_noalloc(FAKE, FAKE, FAKE, 16, 256, found, 4, 12, 256, FAKE, None) == -7

@@ -32,6 +32,7 @@ SIGNATURES = {
     "trellis_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "trellis_gemm_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "trellis_gemm_ws": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "trellis_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
 }
 
 
