@@ -3,37 +3,45 @@
 // Flat view: a (row, block) pair is one "item" of T = 256 weights.  Because
 // codes and the output are both row-major with K a multiple of T, item i
 // reads words [i*wpb, (i+1)*wpb) of `codes` and writes weights
-// [i*256, (i+1)*256) of `out`.  One warp decodes 4 items per step: lane l works
-// on item (step*4 + l/8), group g = l%8 (32 weights).  The lookahead word of a
-// group is the first word of group g-1, which lane l-1 holds (lane l+7 for
-// g = 0, whose window tails wrap to word 0 of the block), so it comes by one
-// shuffle.  Each lane writes its 32 weights as 64 contiguous bytes.
+// [i*256, (i+1)*256) of `out`.  One warp decodes 4 consecutive items per step:
+// lane l works on item (step*4 + l/8), group g = l%8 (32 weights).  The
+// lookahead word of a group is the first word of group g-1, which lane l-1
+// holds (lane l+7 for g = 0, whose window tails wrap to word 0 of the block),
+// so it comes by one shuffle.
 //
-// Bound: HBM.  Per item it reads 32*k bytes and writes 512 bytes; the decode is
-// about 10 integer/fp32 instructions per weight, below the HBM time on GB300.
+// Stores: each lane's 32 weights (64 bytes) go to a per-warp shared-memory
+// buffer laid out exactly like the warp's 2 KB of output, and one lane hands
+// the buffer to the TMA engine as a single bulk copy (cp.async.bulk), double
+// buffered.  The next step's codes are loaded before the current step is
+// decoded.
+//
+// Bound: HBM.  Per item it reads 32*k bytes and writes 512 bytes.
 #include "kernels.h"
 #include "trellis_device.cuh"
 
 namespace trellis {
 
+constexpr int kDecodeWarps = 8;
+constexpr int kDecodeStageBytes = 4 * kT * 2;   // 4 items of bf16 = 2 KB per warp and buffer
+
 template <int KB>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
               uint32_t items, FastDiv blocks_per_row, uint16_t* __restrict__ out) {
     constexpr int WPB = kGroupsPerBlock * KB;
+    __shared__ __align__(128) unsigned char stage[kDecodeWarps][2][kDecodeStageBytes];
+
     const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
     const int g = lane & 7;
     const int sub = lane >> 3;
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     const int src_lane = (g == 0) ? lane + 7 : lane - 1;
 
-    for (uint32_t base = warp * 4u; base < items; base += nwarps * 4u) {
+    auto load = [&](uint32_t base, uint32_t (&w)[KB], float& s) {
         const uint32_t item = base + sub;
-        const bool valid = item < items;
-        uint32_t w[KB + 1];
-        float s = 0.0f;
-        if (valid) {
+        if (item < items) {
             const uint32_t* p = codes + static_cast<size_t>(item) * WPB + (kGroupsPerBlock - 1 - g) * KB;
             if constexpr (KB == 4) {
                 const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
@@ -49,22 +57,69 @@ decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ s
         } else {
 #pragma unroll
             for (int i = 0; i < KB; ++i) w[i] = 0u;
+            s = 0.0f;
         }
+    };
+
+    uint32_t cw[KB];
+    float cs = 0.0f;
+    uint32_t base = warp * 4u;
+    if (base < items) load(base, cw, cs);
+    int buf = 0;
+    const uint32_t stage_lane =
+        static_cast<uint32_t>(__cvta_generic_to_shared(&stage[wib][0][0])) + static_cast<uint32_t>(lane) * 64u;
+
+    for (; base < items; base += nwarps * 4u) {
+        const uint32_t next = base + nwarps * 4u;
+        uint32_t nw[KB];
+        float ns = 0.0f;
+        if (next < items) {
+            load(next, nw, ns);
+        } else {
+#pragma unroll
+            for (int i = 0; i < KB; ++i) nw[i] = 0u;
+        }
+
+        uint32_t w[KB + 1];
+#pragma unroll
+        for (int i = 0; i < KB; ++i) w[i] = cw[i];
         w[KB] = __shfl_sync(0xffffffffu, w[0], src_lane);
-        if (!valid) continue;
 
         uint32_t packed[16];
 #pragma unroll
         for (int jp = 0; jp < 16; ++jp) {
-            const float a = __fmul_rn(window_value(group_window<KB>(w, 2 * jp)), s);
-            const float b = __fmul_rn(window_value(group_window<KB>(w, 2 * jp + 1)), s);
+            const float a = __fmul_rn(window_value(group_window<KB>(w, 2 * jp)), cs);
+            const float b = __fmul_rn(window_value(group_window<KB>(w, 2 * jp + 1)), cs);
             packed[jp] = pack_bf16x2(a, b);
         }
-        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(item) * kT + 32 * g);
+
+        // The bulk copy issued two steps ago from this buffer must have read it.
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+        const uint32_t dst = stage_lane + static_cast<uint32_t>(buf) * kDecodeStageBytes;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         :: "r"(dst + q * 16u), "r"(packed[4 * q]), "r"(packed[4 * q + 1]),
+                            "r"(packed[4 * q + 2]), "r"(packed[4 * q + 3]) : "memory");
+        // make the generic-proxy stores visible to the bulk copy (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t nvalid = (items - base) < 4u ? (items - base) : 4u;
+            uint16_t* gdst = out + static_cast<size_t>(base) * kT;
+            const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(&stage[wib][buf][0]));
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                         :: "l"(gdst), "r"(src), "r"(nvalid * static_cast<uint32_t>(kT * 2)) : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        buf ^= 1;
+#pragma unroll
+        for (int i = 0; i < KB; ++i) cw[i] = nw[i];
+        cs = ns;
     }
+    // the shared buffers must outlive the bulk copies that read them
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
@@ -73,14 +128,14 @@ int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, i
     const uint64_t items64 = static_cast<uint64_t>(N) * blocks_per_row;
     const uint32_t items = static_cast<uint32_t>(items64);
     const uint32_t warps_needed = (items + 3u) / 4u;
-    const uint32_t ctas_needed = (warps_needed + 7u) / 8u;
-    const uint32_t max_ctas = static_cast<uint32_t>(dev.num_sms) * 8u;
+    const uint32_t ctas_needed = (warps_needed + kDecodeWarps - 1u) / kDecodeWarps;
+    const uint32_t max_ctas = static_cast<uint32_t>(dev.num_sms) * 6u;
     const uint32_t grid = ctas_needed < max_ctas ? ctas_needed : max_ctas;
     const FastDiv fd(blocks_per_row);
     switch (k) {
-        case 2: decode_kernel<2><<<grid, 256, 0, stream>>>(codes, scales, items, fd, out); break;
-        case 3: decode_kernel<3><<<grid, 256, 0, stream>>>(codes, scales, items, fd, out); break;
-        case 4: decode_kernel<4><<<grid, 256, 0, stream>>>(codes, scales, items, fd, out); break;
+        case 2: decode_kernel<2><<<grid, kDecodeWarps * 32, 0, stream>>>(codes, scales, items, fd, out); break;
+        case 3: decode_kernel<3><<<grid, kDecodeWarps * 32, 0, stream>>>(codes, scales, items, fd, out); break;
+        case 4: decode_kernel<4><<<grid, kDecodeWarps * 32, 0, stream>>>(codes, scales, items, fd, out); break;
         default: return -3;
     }
     return cudaGetLastError() == cudaSuccess ? 0 : -5;

@@ -7,8 +7,9 @@ namespace trellis {
 // 0 when the geometry needs more tile counters than the workspace layout holds.
 template <int MM>
 static size_t ws_bytes_for(int K, int N, int k, const DeviceInfo& dev) {
-    const SmallMPlan p = plan_smallm<MM>(K, N, k, dev);
-    return smallm_fits_counters<MM>(p) ? smallm_workspace_bytes<MM>(p) : 0;
+    using C = typename SmallMDefault<MM>::type;
+    const SmallMPlan p = plan_smallm<C>(K, N, k, dev);
+    return smallm_fits_counters<C>(p) ? smallm_workspace_bytes<C>(p) : 0;
 }
 
 size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo& dev) {

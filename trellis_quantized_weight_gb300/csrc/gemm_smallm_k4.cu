@@ -10,7 +10,7 @@ int launch_smallm_k<4>(int M, const uint16_t* x, const uint32_t* codes, const ui
                        const DeviceInfo& dev) {
     switch (M) {
 #define TRELLIS_CASE(MV) \
-    case MV: return launch_smallm_instance<MV, 4>(x, codes, scales, K, N, out, ws, ws_bytes, stream, dev);
+    case MV: return launch_smallm_instance<typename SmallMDefault<MV>::type, 4>(x, codes, scales, K, N, out, ws, ws_bytes, stream, dev);
         TRELLIS_CASE(1) TRELLIS_CASE(2) TRELLIS_CASE(3) TRELLIS_CASE(4)
         TRELLIS_CASE(5) TRELLIS_CASE(6) TRELLIS_CASE(7) TRELLIS_CASE(8)
         TRELLIS_CASE(9) TRELLIS_CASE(10) TRELLIS_CASE(11) TRELLIS_CASE(12)

@@ -6,25 +6,34 @@
 // once and share it across every activation row).
 //
 // Mapping (GB300-first, not the page's simdgroup layout):
-//  * lane = output row.  A warp owns a "tile" of 32*R rows (lane l holds rows
-//    l, l+32, ...), so all lanes of a warp sit at the same k at the same time
-//    and every activation value it needs is one broadcast shared-memory read,
-//    reused by the R rows and both weights of an f32x2 FMA.
-//  * WARPS tiles form a "tile-group".  Work units are (tile-group, 32-wide
-//    k-group) pairs, numbered tile-group-major, and CTA c takes the contiguous
+//  * A warp's 32 lanes are 4 row slots x 8 groups: lane l decodes group
+//    g = l%8 (32 weights) of the rows held by slot q = l/8.  The 8 lanes of a
+//    slot read one row's 32*k-byte block together, so a warp-wide code load
+//    touches 4 cache lines, and the lookahead word of group g (the first word
+//    of group g-1, or word 0 of the block for g = 0) arrives by one shuffle.
+//  * Each lane holds R rows (slot q: rows q, q+4, ...), so a warp's tile is
+//    4*R rows and every activation value a lane loads from shared memory feeds
+//    R rows and both weights of an f32x2 FMA.
+//  * WARPS tiles form a "tile-group".  Work units are (tile-group, 256-weight
+//    block) pairs, numbered tile-group-major, and CTA c takes the contiguous
 //    unit range [c*U/P, (c+1)*U/P): every SM gets the same number of weights
-//    whatever N and K are (stream-K split), and all warps of a CTA walk the
-//    same k-groups, so the CTA stages the matching slice of x once, as fp32,
-//    in shared memory.
-//  * A row whose K-range is split over several CTAs writes fp32 partial sums
-//    to the workspace; the last CTA to finish a tile (ticket from a per-tile
-//    counter) adds the partials in CTA order, rounds to bf16, stores and resets
-//    the counter.  The sum order is therefore fixed: identical inputs give
-//    identical bits.  No CTA ever waits on another.
-//  * Decode per weight: funnel shift + mask, hash IMAD, dp4a byte sum into a
-//    float, the 3-op residual-corrected quotient, the scale multiply and a
-//    bf16 round that keeps fp32 format; then MM/2 packed f32x2 FMAs per weight
-//    pair per activation row.
+//    whatever N and K are (stream-K split).  All warps of a CTA walk the same
+//    blocks in step, so the CTA stages x one block ahead, as fp32, through a
+//    two-slot shared-memory ring ([group][k-pair][m][2], groups padded by 16
+//    bytes so the 8 groups of a load hit 8 different bank quads), with one
+//    CTA barrier per block.
+//  * At the end of a row segment the 8 lanes of a slot add their per-group
+//    sums by butterfly shuffles.  A row whose K-range is split over several
+//    CTAs writes fp32 partial sums to the workspace; the last CTA to finish a
+//    tile (ticket from a per-tile counter) adds the partials in CTA order,
+//    rounds to bf16, stores and resets the counter.  The sum order is fixed:
+//    identical inputs give identical bits.  No CTA ever waits on another.
+//  * Decode per weight: funnel shift + mask, hash IMAD, then either the dp4a
+//    byte sum into a float and the 3-op residual-corrected quotient, or one
+//    dp4a that turns the hash into the address of the quotient in a per-lane
+//    shared-memory table (one conflict-free load).  Then a packed f32x2 scale
+//    multiply, a bf16 round that keeps fp32 format, and MM packed f32x2 FMAs
+//    per weight pair and row (two k at once).
 #pragma once
 
 #include <cstdint>
@@ -36,22 +45,43 @@ namespace trellis {
 
 struct SmallMPlan {
     int M, K, N;
-    int G;              // k-groups per row (K / 32)
+    int nblocks;        // 256-weight blocks per row (K / 256)
     int row_words;      // K * k / 32
     int ntg;            // tile-groups
     int P;              // CTAs
     int units_max;      // ceil(U / P)
-    long long U;        // units = ntg * G
-    float* partials;    // workspace: [P][2][WARPS][M][R][32] fp32
+    long long U;        // units = ntg * nblocks
+    float* partials;    // workspace: [P][2][WARPS][R*M*4] fp32
     uint32_t* counters; // workspace: [ntg * WARPS]
 };
 
-template <int MM>
-struct SmallMShape {
-    static constexpr int R = 2;                       // rows per lane
-    static constexpr int WARPS = (MM <= 8) ? 16 : 8;  // warps per CTA = tiles per tile-group
+// Compile-time shape of one instantiation.
+//   R      rows per lane (a warp's tile is 4*R rows)
+//   WARPS  warps per CTA (= tiles per tile-group)
+//   LUT    decode the quotient through a shared-memory table instead of the
+//          three-op residual correction (same bits either way)
+template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1>
+struct SmallMCfg {
+    static constexpr int MM = MM_;
+    static constexpr int R = R_;
+    static constexpr int WARPS = WARPS_;
+    static constexpr bool LUT = LUT_;
+    static constexpr int OCC = OCC_;                              // CTAs per SM
     static constexpr int MP = (MM == 1) ? 1 : ((MM + 1) & ~1);   // padded x rows in smem
-    static constexpr int XS_UNIT = 32 * MP;           // floats of staged x per k-group
+    static constexpr int XG = 32 * MP + 4;                        // floats per staged (block, group)
+    static constexpr int XS_UNIT = 8 * XG;                        // floats of staged x per block
+    static constexpr int TABLE_BYTES = LUT ? kQuotientTableBytes : 0;
+    static constexpr int ROWS_PER_TILE = 4 * R;
+    static constexpr int NT = WARPS * 32;
+    static constexpr int XPT = (MP * 256 + NT - 1) / NT;          // x elements staged per thread per block
+    static constexpr size_t SMEM_BYTES = TABLE_BYTES + 2 * XS_UNIT * sizeof(float);
+};
+
+// The shape used by the library for each M (chosen by timing the M = 1, 5, 8
+// and 15 workloads on GB300 over R, WARPS, LUT and CTAs per SM).
+template <int MM>
+struct SmallMDefault {
+    using type = SmallMCfg<MM, (MM <= 5) ? 4 : (MM <= 8 ? 3 : 2), (MM <= 11) ? 16 : 8, (MM <= 5)>;
 };
 
 __device__ __forceinline__ int cta_of_unit(long long u, long long U, int P) {
@@ -59,91 +89,145 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long U, int P) {
     return static_cast<int>(c < P - 1 ? c : P - 1);
 }
 
-template <int MM, int KB>
-__global__ void __launch_bounds__(SmallMShape<MM>::WARPS * 32, 1)
+template <int KB, int R>
+__device__ __forceinline__ void load_block_group(const uint32_t* const (&rp)[R], const bool (&ok)[R], int b,
+                                                 int g, uint32_t (&w)[R][KB]) {
+    constexpr int WPB = kGroupsPerBlock * KB;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (ok[r]) {
+            const uint32_t* p = rp[r] + b * WPB + (kGroupsPerBlock - 1 - g) * KB;
+            if constexpr (KB == 4) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+                w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
+            } else if constexpr (KB == 2) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+                w[r][0] = v.x; w[r][1] = v.y;
+            } else {
+#pragma unroll
+                for (int i = 0; i < KB; ++i) w[r][i] = __ldg(p + i);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < KB; ++i) w[r][i] = 0u;
+        }
+    }
+}
+
+// x of one 256-weight block: each thread loads its XPT elements (bf16) ...
+template <class C>
+__device__ __forceinline__ void x_block_load(const uint16_t* __restrict__ x, int K, int b, int tid,
+                                             uint16_t (&v)[C::XPT]) {
+#pragma unroll
+    for (int i = 0; i < C::XPT; ++i) {
+        const int e = tid + i * C::NT;        // e = m*256 + kk
+        const int m = e >> 8, kk = e & 255;
+        v[i] = (e < C::MP * 256 && m < C::MM) ? __ldg(x + static_cast<size_t>(m) * K + b * 256 + kk)
+                                              : static_cast<uint16_t>(0);
+    }
+}
+
+// ... and stores them as fp32 in the layout [group][k-pair][m][2] of one ring slot.
+template <class C>
+__device__ __forceinline__ void x_block_store(float* slot, int tid, const uint16_t (&v)[C::XPT]) {
+#pragma unroll
+    for (int i = 0; i < C::XPT; ++i) {
+        const int e = tid + i * C::NT;
+        if (e < C::MP * 256) {
+            const int m = e >> 8, kk = e & 255;
+            const int gg = kk >> 5, kl = kk & 31;
+            slot[gg * C::XG + ((kl >> 1) * C::MP + m) * 2 + (kl & 1)] = bf16_bits_to_f32(v[i]);
+        }
+    }
+}
+
+template <class C, int KB>
+__global__ void __launch_bounds__(C::WARPS * 32, C::OCC)
 gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes,
                    const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, SmallMPlan p) {
-    using S = SmallMShape<MM>;
-    constexpr int R = S::R, WARPS = S::WARPS, MP = S::MP, XS_UNIT = S::XS_UNIT;
-    constexpr int WPB = kGroupsPerBlock * KB;
-    constexpr int NT = WARPS * 32;
-    extern __shared__ __align__(16) float xs[];
+    constexpr int MM = C::MM, R = C::R, WARPS = C::WARPS, MP = C::MP, XG = C::XG, XS_UNIT = C::XS_UNIT;
+    constexpr int NT = C::NT;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float* xs = reinterpret_cast<float*>(smem_raw + C::TABLE_BYTES);   // 2 ring slots of XS_UNIT floats
 
     const int c = blockIdx.x;
     const long long u0 = static_cast<long long>(c) * p.U / p.P;
     const long long u1 = static_cast<long long>(c + 1) * p.U / p.P;
-    const int nunits = static_cast<int>(u1 - u0);
     const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g = lane & 7, slot = lane >> 3;
+    const int src_lane = (g == 0) ? lane + 7 : lane - 1;
+    const int first_tg = static_cast<int>(u0 / p.nblocks);
 
-    // ---- stage x for this CTA's k-groups: xs[q][kk/2][m][kk%2] (fp32) ----
-    for (int q = 0; q < nunits; ++q) {
-        const int k0 = static_cast<int>((u0 + q) % p.G) * 32;
-        float* xq = xs + q * XS_UNIT;
-        for (int e = tid; e < MP * 32; e += NT) {
-            const int m = e >> 5, kk = e & 31;
-            float v = 0.0f;
-            if (m < MM) v = bf16_bits_to_f32(x[static_cast<size_t>(m) * p.K + k0 + kk]);
-            xq[((kk >> 1) * MP + m) * 2 + (kk & 1)] = v;   // MP == 1 gives xq[kk]
-        }
+    if constexpr (C::LUT) build_quotient_table(reinterpret_cast<float*>(smem_raw), tid, NT);
+    const uint32_t lane_tbl = quotient_table_lane_address(smem_raw, lane);
+
+    // Stage x of the first unit into ring slot 0.
+    if (u0 < u1) {
+        uint16_t xv0[C::XPT];
+        x_block_load<C>(x, p.K, static_cast<int>(u0 % p.nblocks), tid, xv0);
+        x_block_store<C>(xs, tid, xv0);
     }
     __syncthreads();
 
-    const int warp = tid >> 5, lane = tid & 31;
-    const int first_tg = static_cast<int>(u0 / p.G);
+    // Per-segment state of this warp's tile.
+    bool ok[R];
+    float2 s2[R];
+    const uint32_t* rp[R];
+    float2 acc[R][MM];
+    uint32_t cw[R][KB];
+    int tg = -1, row0 = 0, tile = 0, b_first = 0;
+    bool live = false;
 
-    for (long long u = u0; u < u1;) {
-        const int tg = static_cast<int>(u / p.G);
-        const int j0 = static_cast<int>(u - static_cast<long long>(tg) * p.G);
-        const long long rest = u1 - u;
-        const int len = static_cast<int>((p.G - j0) < rest ? (p.G - j0) : rest);
-        const int j1 = j0 + len;
-        const int q0 = static_cast<int>(u - u0);
-        u += len;
+    for (long long u = u0; u < u1; ++u) {
+        const int ring = static_cast<int>(u - u0) & 1;
+        const int utg = static_cast<int>(u / p.nblocks);
+        const int b = static_cast<int>(u - static_cast<long long>(utg) * p.nblocks);
+        const bool seg_start = (u == u0) || (b == 0);
+        const bool seg_end = (u + 1 == u1) || (b + 1 == p.nblocks);
 
-        const int tile = tg * WARPS + warp;
-        const int row0 = tile * 32 * R;
-        if (row0 >= p.N) continue;   // whole tile beyond N: skipped by every CTA alike
+        // x of the next unit: loads now, shared stores after this unit's work
+        uint16_t xnext[C::XPT];
+        const bool have_next = u + 1 < u1;
+        if (have_next) x_block_load<C>(x, p.K, static_cast<int>((u + 1) % p.nblocks), tid, xnext);
 
-        bool ok[R];
-        float s[R];
-        const uint32_t* rp[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int n = row0 + 32 * r + lane;
-            ok[r] = n < p.N;
-            s[r] = ok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
-            rp[r] = codes + static_cast<size_t>(ok[r] ? n : 0) * p.row_words;
-        }
-
-        float2 acc[R][MM];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int m = 0; m < MM; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
-
-        uint32_t cur[R][KB + 1], nxt[R][KB + 1];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (ok[r]) {
-                load_group_words<KB>(rp[r] + (j0 >> 3) * WPB, j0 & 7, cur[r]);
-            } else {
-#pragma unroll
-                for (int i = 0; i <= KB; ++i) cur[r][i] = 0u;
-            }
-        }
-
-        for (int j = j0; j < j1; ++j) {
-            const int jn = j + 1;
+        if (seg_start) {
+            tg = utg;
+            b_first = b;
+            tile = tg * WARPS + warp;
+            row0 = tile * C::ROWS_PER_TILE;
+            live = row0 < p.N;   // whole tile beyond N: skipped by every CTA alike
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                if (ok[r] && jn < j1) {
-                    load_group_words<KB>(rp[r] + (jn >> 3) * WPB, jn & 7, nxt[r]);
-                } else {
+                const int n = row0 + slot + 4 * r;
+                ok[r] = n < p.N;
+                const float sr = ok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
+                s2[r] = make_float2(sr, sr);
+                rp[r] = codes + static_cast<size_t>(ok[r] ? n : 0) * p.row_words;
 #pragma unroll
-                    for (int i = 0; i <= KB; ++i) nxt[r][i] = 0u;
-                }
+                for (int m = 0; m < MM; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
             }
-            const float* xq = xs + (q0 + (j - j0)) * XS_UNIT;
+            if (live) load_block_group<KB, R>(rp, ok, b, g, cw);
+        }
+
+        if (live) {
+            uint32_t nw[R][KB];
+            if (!seg_end) {
+                load_block_group<KB, R>(rp, ok, b + 1, g, nw);
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int i = 0; i < KB; ++i) nw[r][i] = 0u;
+            }
+            uint32_t w[R][KB + 1];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+#pragma unroll
+                for (int i = 0; i < KB; ++i) w[r][i] = cw[r][i];
+                w[r][KB] = __shfl_sync(0xffffffffu, cw[r][0], src_lane);
+            }
+            const float* xq = xs + ring * XS_UNIT + g * XG;
 #pragma unroll
             for (int pp = 0; pp < 16; ++pp) {
                 float2 xv[MM];
@@ -159,11 +243,16 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 }
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const float wa = round_bf16_as_f32(
-                        __fmul_rn(window_value(group_window<KB>(cur[r], 2 * pp)), s[r]));
-                    const float wb = round_bf16_as_f32(
-                        __fmul_rn(window_value(group_window<KB>(cur[r], 2 * pp + 1)), s[r]));
-                    const float2 wv = make_float2(wa, wb);
+                    float2 v;
+                    if constexpr (C::LUT) {
+                        v.x = quotient_lookup(group_window<KB>(w[r], 2 * pp), lane_tbl);
+                        v.y = quotient_lookup(group_window<KB>(w[r], 2 * pp + 1), lane_tbl);
+                    } else {
+                        v.x = window_value(group_window<KB>(w[r], 2 * pp));
+                        v.y = window_value(group_window<KB>(w[r], 2 * pp + 1));
+                    }
+                    const float2 ws = __fmul2_rn(v, s2[r]);
+                    const float2 wv = make_float2(round_bf16_as_f32(ws.x), round_bf16_as_f32(ws.y));
 #pragma unroll
                     for (int m = 0; m < MM; ++m) acc[r][m] = __ffma2_rn(wv, xv[m], acc[r][m]);
                 }
@@ -171,93 +260,77 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int i = 0; i <= KB; ++i) cur[r][i] = nxt[r][i];
+                for (int i = 0; i < KB; ++i) cw[r][i] = nw[r][i];
         }
 
-        float v[R][MM];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int m = 0; m < MM; ++m) v[r][m] = __fadd_rn(acc[r][m].x, acc[r][m].y);
-
-        if (j0 == 0 && j1 == p.G) {
-            // this CTA owns the whole K-range of the tile-group
+        if (live && seg_end) {
+            // ---- per-row sums: k-pair halves, then the 8 groups of the slot ----
+            float v[R][MM];
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                if (ok[r])
 #pragma unroll
-                    for (int m = 0; m < MM; ++m)
-                        out[static_cast<size_t>(m) * p.N + row0 + 32 * r + lane] =
-                            bf16_bits_rn(v[r][m]);
-            continue;
-        }
+                for (int m = 0; m < MM; ++m) {
+                    float t = __fadd_rn(acc[r][m].x, acc[r][m].y);
+                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 1));
+                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 2));
+                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 4));
+                    v[r][m] = t;   // identical in the 8 lanes of the slot
+                }
 
-        // ---- split row: publish the partial, the last arriver reduces ----
-        const int slot = (tg == first_tg) ? 0 : 1;
-        float* mine = p.partials + ((static_cast<size_t>(c) * 2 + slot) * WARPS + warp) * (MM * R * 32);
-#pragma unroll
-        for (int m = 0; m < MM; ++m)
-#pragma unroll
-            for (int r = 0; r < R; ++r) mine[(m * R + r) * 32 + lane] = v[r][m];
-        __threadfence();
-        __syncwarp();
-        uint32_t ticket = 0;
-        if (lane == 0) ticket = atomicAdd(p.counters + tile, 1u);
-        ticket = __shfl_sync(0xffffffffu, ticket, 0);
-        const long long tg_u0 = static_cast<long long>(tg) * p.G;
-        const int c_first = cta_of_unit(tg_u0, p.U, p.P);
-        const int c_last = cta_of_unit(tg_u0 + p.G - 1, p.U, p.P);
-        if (ticket != static_cast<uint32_t>(c_last - c_first)) continue;
-
-        __threadfence();
-        float sum[R][MM];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int m = 0; m < MM; ++m) sum[r][m] = 0.0f;
-        for (int cc = c_first; cc <= c_last; ++cc) {
-            const long long cc_u0 = static_cast<long long>(cc) * p.U / p.P;
-            const int cc_slot = (tg == static_cast<int>(cc_u0 / p.G)) ? 0 : 1;
-            const float* src =
-                p.partials + ((static_cast<size_t>(cc) * 2 + cc_slot) * WARPS + warp) * (MM * R * 32);
-#pragma unroll
-            for (int m = 0; m < MM; ++m)
+            if (b_first == 0 && b + 1 == p.nblocks) {
+                // this CTA owns the whole K-range of the tile-group; lane g of a
+                // slot stores the outputs m with m % 8 == g
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    sum[r][m] = __fadd_rn(sum[r][m], __ldcg(src + (m * R + r) * 32 + lane));
+                    if (ok[r])
+#pragma unroll
+                        for (int m = 0; m < MM; ++m)
+                            if ((m & 7) == g)
+                                out[static_cast<size_t>(m) * p.N + row0 + slot + 4 * r] = bf16_bits_rn(v[r][m]);
+            } else {
+                // ---- split row: publish the partial, the last arriver reduces ----
+                // element (r, m) of row slot q sits at [(r*MM + m)*4 + q]; lane g == 0 writes
+                const int pslot = (tg == first_tg) ? 0 : 1;
+                float* mine = p.partials + ((static_cast<size_t>(c) * 2 + pslot) * WARPS + warp) * (R * MM * 4);
+                if (g == 0) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+#pragma unroll
+                        for (int m = 0; m < MM; ++m) mine[(r * MM + m) * 4 + slot] = v[r][m];
+                }
+                __threadfence();
+                __syncwarp();
+                uint32_t ticket = 0;
+                if (lane == 0) ticket = atomicAdd(p.counters + tile, 1u);
+                ticket = __shfl_sync(0xffffffffu, ticket, 0);
+                const long long tg_u0 = static_cast<long long>(tg) * p.nblocks;
+                const int c_first = cta_of_unit(tg_u0, p.U, p.P);
+                const int c_last = cta_of_unit(tg_u0 + p.nblocks - 1, p.U, p.P);
+                if (ticket == static_cast<uint32_t>(c_last - c_first)) {
+                    __threadfence();
+                    // the 32 lanes share the R*MM*4 sums of the tile
+                    for (int e = lane; e < R * MM * 4; e += 32) {
+                        float sum = 0.0f;
+                        for (int cc = c_first; cc <= c_last; ++cc) {
+                            const long long cc_u0 = static_cast<long long>(cc) * p.U / p.P;
+                            const int cc_slot = (tg == static_cast<int>(cc_u0 / p.nblocks)) ? 0 : 1;
+                            const float* src = p.partials +
+                                ((static_cast<size_t>(cc) * 2 + cc_slot) * WARPS + warp) * (R * MM * 4);
+                            sum = __fadd_rn(sum, __ldcg(src + e));
+                        }
+                        const int q = e & 3, rm = e >> 2;
+                        const int r = rm / MM, m = rm - r * MM;
+                        const int n = row0 + q + 4 * r;
+                        if (n < p.N) out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum);
+                    }
+                    if (lane == 0) p.counters[tile] = 0u;
+                }
+            }
         }
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            if (ok[r])
-#pragma unroll
-                for (int m = 0; m < MM; ++m)
-                    out[static_cast<size_t>(m) * p.N + row0 + 32 * r + lane] =
-                        bf16_bits_rn(sum[r][m]);
-        if (lane == 0) p.counters[tile] = 0u;
-    }
-}
 
-// Host-side planning shared by the per-k instantiation files.
-template <int MM>
-SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev) {
-    using S = SmallMShape<MM>;
-    SmallMPlan p{};
-    p.M = MM;
-    p.K = K;
-    p.N = N;
-    p.G = K / 32;
-    p.row_words = K / 32 * k;
-    const int rows_per_tg = S::WARPS * 32 * S::R;
-    p.ntg = (N + rows_per_tg - 1) / rows_per_tg;
-    p.U = static_cast<long long>(p.ntg) * p.G;
-    long long P = dev.num_sms;
-    if (P > p.U) P = p.U;
-    const long long bytes_per_unit = static_cast<long long>(S::XS_UNIT) * 4;
-    const long long ucap = dev.max_smem_optin / bytes_per_unit;
-    if ((p.U + P - 1) / P > ucap) P = (p.U + ucap - 1) / ucap;
-    p.P = static_cast<int>(P);
-    p.units_max = static_cast<int>((p.U + P - 1) / P);
-    return p;
+        if (have_next) x_block_store<C>(xs + (ring ^ 1) * XS_UNIT, tid, xnext);
+        __syncthreads();
+    }
 }
 
 // Workspace layout: a fixed-capacity counter region at offset 0 (the same
@@ -267,38 +340,55 @@ SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev) {
 constexpr size_t kCounterCapacity = size_t(1) << 18;            // tiles
 constexpr size_t kCounterBytes = kCounterCapacity * sizeof(uint32_t);
 
-template <int MM>
+// Host-side planning.
+template <class C>
+SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev) {
+    SmallMPlan p{};
+    p.M = C::MM;
+    p.K = K;
+    p.N = N;
+    p.nblocks = K / 256;
+    p.row_words = K / 32 * k;
+    const int rows_per_tg = C::WARPS * C::ROWS_PER_TILE;
+    p.ntg = (N + rows_per_tg - 1) / rows_per_tg;
+    p.U = static_cast<long long>(p.ntg) * p.nblocks;
+    long long P = static_cast<long long>(dev.num_sms) * C::OCC;
+    if (P > p.U) P = p.U;
+    p.P = static_cast<int>(P);
+    p.units_max = static_cast<int>((p.U + P - 1) / P);
+    return p;
+}
+
+template <class C>
 size_t smallm_workspace_bytes(const SmallMPlan& p) {
-    using S = SmallMShape<MM>;
-    const size_t partials = static_cast<size_t>(p.P) * 2 * S::WARPS * MM * S::R * 32 * 4;
+    const size_t partials = static_cast<size_t>(p.P) * 2 * C::WARPS * C::R * C::MM * 4 * sizeof(float);
     return kCounterBytes + partials;
 }
 
-template <int MM>
+template <class C>
 bool smallm_fits_counters(const SmallMPlan& p) {
-    return static_cast<size_t>(p.ntg) * SmallMShape<MM>::WARPS <= kCounterCapacity;
+    return static_cast<size_t>(p.ntg) * C::WARPS <= kCounterCapacity;
 }
 
-template <int MM, int KB>
+template <class C, int KB>
 int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales,
                            int K, int N, uint16_t* out, void* ws, size_t ws_bytes,
                            cudaStream_t stream, const DeviceInfo& dev) {
-    using S = SmallMShape<MM>;
-    SmallMPlan p = plan_smallm<MM>(K, N, KB, dev);
-    if (!smallm_fits_counters<MM>(p)) return -2;
-    const size_t need = smallm_workspace_bytes<MM>(p);
+    SmallMPlan p = plan_smallm<C>(K, N, KB, dev);
+    if (!smallm_fits_counters<C>(p)) return -2;
+    const size_t need = smallm_workspace_bytes<C>(p);
     if (ws_bytes < need || ws == nullptr) return -7;
     p.counters = static_cast<uint32_t*>(ws);
     p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
-    const size_t smem = static_cast<size_t>(p.units_max) * S::XS_UNIT * 4;
+    const size_t smem = C::SMEM_BYTES;
     static bool attr_set = false;   // idempotent; a race only repeats the call
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_smallm_kernel<MM, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 dev.max_smem_optin) != cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_smallm_kernel<C, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(C::SMEM_BYTES)) != cudaSuccess)
             return -5;
         attr_set = true;
     }
-    gemm_smallm_kernel<MM, KB><<<p.P, S::WARPS * 32, smem, stream>>>(x, codes, scales, out, p);
+    gemm_smallm_kernel<C, KB><<<p.P, C::WARPS * 32, smem, stream>>>(x, codes, scales, out, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 

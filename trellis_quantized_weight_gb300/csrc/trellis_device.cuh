@@ -49,14 +49,50 @@ __device__ __forceinline__ uint32_t group_window(const uint32_t (&w)[KB + 1], in
     return win & ((1u << kL) - 1u);
 }
 
+// float(code) -> code / 147.800537109375 rounded to nearest fp32, by the
+// page's residual correction: q0 = code*r, e = code - q0*c (exact in one FMA),
+// q = q0 + e*r.  For every integer code in [-510, 510] this is the correctly
+// rounded quotient (checked exhaustively against exact rational arithmetic).
+__device__ __forceinline__ float code_to_value(float code) {
+    const float approx = __fmul_rn(code, kRecip);
+    const float residual = __fmaf_rn(-approx, kDivisor, code);
+    return __fmaf_rn(residual, kRecip, approx);
+}
+
 // 12-bit window -> fp32 value, bit-exact with code / 147.800537109375.
 __device__ __forceinline__ float window_value(uint32_t win) {
     const uint32_t z = win * kHashMul + kHashAdd;
     const float biased = __uint_as_float(__dp4a(z, 0x01010101u, kMagicBits));
-    const float code = __fsub_rn(biased, kMagicPlusBias);
-    const float approx = __fmul_rn(code, kRecip);
-    const float residual = __fmaf_rn(-approx, kDivisor, code);
-    return __fmaf_rn(residual, kRecip, approx);
+    return code_to_value(__fsub_rn(biased, kMagicPlusBias));
+}
+
+// ---- quotient table ---------------------------------------------------------
+// The value depends on the window only through the byte sum S = code + 510,
+// S in [0, 1020].  A shared-memory table holds value(S) once per lane:
+// entry (S, lane) sits at byte 128*S + 4*lane, so the 32 lanes of a warp always
+// read 32 different banks, whatever their S.  dp4a(z, 0x80808080, base) yields
+// base + 128*S directly, so a lookup is one dp4a and one shared load.
+constexpr int kByteSums = 1021;
+constexpr int kQuotientTableBytes = kByteSums * 32 * 4;   // 130,688 bytes
+
+__device__ __forceinline__ void build_quotient_table(float* table, int tid, int nthreads) {
+    for (int e = tid; e < kByteSums * 8; e += nthreads) {
+        const int sum = e >> 3, quad = e & 7;
+        const float v = code_to_value(static_cast<float>(sum - 510));
+        *reinterpret_cast<float4*>(table + sum * 32 + quad * 4) = make_float4(v, v, v, v);
+    }
+}
+
+__device__ __forceinline__ uint32_t quotient_table_lane_address(const void* table, int lane) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(table)) + 4u * static_cast<uint32_t>(lane);
+}
+
+__device__ __forceinline__ float quotient_lookup(uint32_t win, uint32_t lane_address) {
+    const uint32_t z = win * kHashMul + kHashAdd;
+    const uint32_t addr = __dp4a(z, 0x80808080u, lane_address);
+    float v;
+    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
 }
 
 // bf16 round-to-nearest-even of w, returned as the fp32 with the same value
