@@ -19,9 +19,9 @@
 //    unit range [c*U/P, (c+1)*U/P): every SM gets the same number of weights
 //    whatever N and K are (stream-K split).  All warps of a CTA walk the same
 //    blocks in step, so the CTA stages x one block ahead, as fp32, through a
-//    two-slot shared-memory ring ([group][k-pair][m][2], groups padded by 16
-//    bytes so the 8 groups of a load hit 8 different bank quads), with one
-//    CTA barrier per block.
+//    two-slot shared-memory ring ([group][m][32 k], groups padded by 16 bytes
+//    so the 8 groups of a load hit 8 different bank quads), with one CTA
+//    barrier per block.
 //  * At the end of a row segment the 8 lanes of a slot add their per-group
 //    sums by butterfly shuffles.  A row whose K-range is split over several
 //    CTAs writes fp32 partial sums to the workspace; the last CTA to finish a
@@ -67,13 +67,13 @@ struct SmallMCfg {
     static constexpr int WARPS = WARPS_;
     static constexpr bool LUT = LUT_;
     static constexpr int OCC = OCC_;                              // CTAs per SM
-    static constexpr int MP = (MM == 1) ? 1 : ((MM + 1) & ~1);   // padded x rows in smem
-    static constexpr int XG = 32 * MP + 4;                        // floats per staged (block, group)
+    static constexpr int XG = 32 * MM + 4;                        // floats per staged (block, group)
     static constexpr int XS_UNIT = 8 * XG;                        // floats of staged x per block
     static constexpr int TABLE_BYTES = LUT ? kQuotientTableBytes : 0;
     static constexpr int ROWS_PER_TILE = 4 * R;
     static constexpr int NT = WARPS * 32;
-    static constexpr int XPT = (MP * 256 + NT - 1) / NT;          // x elements staged per thread per block
+    static constexpr int XV = MM * 32;                            // 8-element x vectors per block
+    static constexpr int XPT = (XV + NT - 1) / NT;                // x vectors staged per thread per block
     static constexpr size_t SMEM_BYTES = TABLE_BYTES + 2 * XS_UNIT * sizeof(float);
 };
 
@@ -81,7 +81,7 @@ struct SmallMCfg {
 // and 15 workloads on GB300 over R, WARPS, LUT and CTAs per SM).
 template <int MM>
 struct SmallMDefault {
-    using type = SmallMCfg<MM, (MM <= 5) ? 4 : (MM <= 8 ? 3 : 2), (MM <= 11) ? 16 : 8, (MM <= 5)>;
+    using type = SmallMCfg<MM, (MM <= 5) ? 4 : 3, (MM <= 7) ? 16 : (MM <= 11 ? 12 : 8), true>;
 };
 
 __device__ __forceinline__ int cta_of_unit(long long u, long long U, int P) {
@@ -114,29 +114,40 @@ __device__ __forceinline__ void load_block_group(const uint32_t* const (&rp)[R],
     }
 }
 
-// x of one 256-weight block: each thread loads its XPT elements (bf16) ...
+// x of one 256-weight block, 8 bf16 (16 bytes) per load: vector i of the
+// block is row m = i/32, columns 8*(i%32) .. +7 ...
 template <class C>
 __device__ __forceinline__ void x_block_load(const uint16_t* __restrict__ x, int K, int b, int tid,
-                                             uint16_t (&v)[C::XPT]) {
-#pragma unroll
-    for (int i = 0; i < C::XPT; ++i) {
-        const int e = tid + i * C::NT;        // e = m*256 + kk
-        const int m = e >> 8, kk = e & 255;
-        v[i] = (e < C::MP * 256 && m < C::MM) ? __ldg(x + static_cast<size_t>(m) * K + b * 256 + kk)
-                                              : static_cast<uint16_t>(0);
-    }
-}
-
-// ... and stores them as fp32 in the layout [group][k-pair][m][2] of one ring slot.
-template <class C>
-__device__ __forceinline__ void x_block_store(float* slot, int tid, const uint16_t (&v)[C::XPT]) {
+                                             uint4 (&v)[C::XPT]) {
 #pragma unroll
     for (int i = 0; i < C::XPT; ++i) {
         const int e = tid + i * C::NT;
-        if (e < C::MP * 256) {
-            const int m = e >> 8, kk = e & 255;
-            const int gg = kk >> 5, kl = kk & 31;
-            slot[gg * C::XG + ((kl >> 1) * C::MP + m) * 2 + (kl & 1)] = bf16_bits_to_f32(v[i]);
+        if (e < C::XV) {
+            const int m = e >> 5, c8 = e & 31;
+            v[i] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(m) * K + b * 256 + c8 * 8));
+        }
+    }
+}
+
+// ... stored as fp32 in the layout [group][m][32 k] of one ring slot (the two
+// floats of a k-pair are adjacent, ready for f32x2 FMAs).
+template <class C>
+__device__ __forceinline__ void x_block_store(float* slot, int tid, const uint4 (&v)[C::XPT]) {
+#pragma unroll
+    for (int i = 0; i < C::XPT; ++i) {
+        const int e = tid + i * C::NT;
+        if (e < C::XV) {
+            const int m = e >> 5, c8 = e & 31;
+            float* dst = slot + (c8 >> 2) * C::XG + m * 32 + (c8 & 3) * 8;
+            const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            float f[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                f[2 * h] = __uint_as_float(u[h] << 16);
+                f[2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
+            }
+            *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
         }
     }
 }
@@ -145,7 +156,7 @@ template <class C, int KB>
 __global__ void __launch_bounds__(C::WARPS * 32, C::OCC)
 gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes,
                    const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, SmallMPlan p) {
-    constexpr int MM = C::MM, R = C::R, WARPS = C::WARPS, MP = C::MP, XG = C::XG, XS_UNIT = C::XS_UNIT;
+    constexpr int MM = C::MM, R = C::R, WARPS = C::WARPS, XG = C::XG, XS_UNIT = C::XS_UNIT;
     constexpr int NT = C::NT;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float* xs = reinterpret_cast<float*>(smem_raw + C::TABLE_BYTES);   // 2 ring slots of XS_UNIT floats
@@ -164,7 +175,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 
     // Stage x of the first unit into ring slot 0.
     if (u0 < u1) {
-        uint16_t xv0[C::XPT];
+        uint4 xv0[C::XPT];
         x_block_load<C>(x, p.K, static_cast<int>(u0 % p.nblocks), tid, xv0);
         x_block_store<C>(xs, tid, xv0);
     }
@@ -187,7 +198,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         const bool seg_end = (u + 1 == u1) || (b + 1 == p.nblocks);
 
         // x of the next unit: loads now, shared stores after this unit's work
-        uint16_t xnext[C::XPT];
+        uint4 xnext[C::XPT];
         const bool have_next = u + 1 < u1;
         if (have_next) x_block_load<C>(x, p.K, static_cast<int>((u + 1) % p.nblocks), tid, xnext);
 
@@ -211,6 +222,14 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         }
 
         if (live) {
+            // the block after next: pull it toward L2 now, so the register
+            // prefetch issued one unit ahead finds it there
+            if (b + 2 < p.nblocks && u + 2 < u1) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (ok[r] && g == 0)
+                        asm volatile("prefetch.global.L2 [%0];" :: "l"(rp[r] + (b + 2) * (kGroupsPerBlock * KB)));
+            }
             uint32_t nw[R][KB];
             if (!seg_end) {
                 load_block_group<KB, R>(rp, ok, b + 1, g, nw);
@@ -229,32 +248,34 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             }
             const float* xq = xs + ring * XS_UNIT + g * XG;
 #pragma unroll
-            for (int pp = 0; pp < 16; ++pp) {
-                float2 xv[MM];
-                if constexpr (MM == 1) {
-                    xv[0] = *reinterpret_cast<const float2*>(xq + 2 * pp);
-                } else {
+            for (int pq = 0; pq < 8; ++pq) {
+                // k-pairs 2pq and 2pq+1 of the group: x[m][4pq .. 4pq+3]
+                float2 xa[MM], xb[MM];
 #pragma unroll
-                    for (int mm = 0; mm < MP / 2; ++mm) {
-                        const float4 t = *reinterpret_cast<const float4*>(xq + (pp * MP + 2 * mm) * 2);
-                        xv[2 * mm] = make_float2(t.x, t.y);
-                        if (2 * mm + 1 < MM) xv[2 * mm + 1] = make_float2(t.z, t.w);
-                    }
+                for (int m = 0; m < MM; ++m) {
+                    const float4 t = *reinterpret_cast<const float4*>(xq + m * 32 + 4 * pq);
+                    xa[m] = make_float2(t.x, t.y);
+                    xb[m] = make_float2(t.z, t.w);
                 }
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float2 v;
-                    if constexpr (C::LUT) {
-                        v.x = quotient_lookup(group_window<KB>(w[r], 2 * pp), lane_tbl);
-                        v.y = quotient_lookup(group_window<KB>(w[r], 2 * pp + 1), lane_tbl);
-                    } else {
-                        v.x = window_value(group_window<KB>(w[r], 2 * pp));
-                        v.y = window_value(group_window<KB>(w[r], 2 * pp + 1));
-                    }
-                    const float2 ws = __fmul2_rn(v, s2[r]);
-                    const float2 wv = make_float2(round_bf16_as_f32(ws.x), round_bf16_as_f32(ws.y));
+                for (int half = 0; half < 2; ++half) {
+                    const int pp = 2 * pq + half;
 #pragma unroll
-                    for (int m = 0; m < MM; ++m) acc[r][m] = __ffma2_rn(wv, xv[m], acc[r][m]);
+                    for (int r = 0; r < R; ++r) {
+                        float2 v;
+                        if constexpr (C::LUT) {
+                            v.x = quotient_lookup(group_window<KB>(w[r], 2 * pp), lane_tbl);
+                            v.y = quotient_lookup(group_window<KB>(w[r], 2 * pp + 1), lane_tbl);
+                        } else {
+                            v.x = window_value(group_window<KB>(w[r], 2 * pp));
+                            v.y = window_value(group_window<KB>(w[r], 2 * pp + 1));
+                        }
+                        const float2 ws = __fmul2_rn(v, s2[r]);
+                        const float2 wv = make_float2(round_bf16_as_f32(ws.x), round_bf16_as_f32(ws.y));
+#pragma unroll
+                        for (int m = 0; m < MM; ++m)
+                            acc[r][m] = __ffma2_rn(wv, half ? xb[m] : xa[m], acc[r][m]);
+                    }
                 }
             }
 #pragma unroll
@@ -308,15 +329,31 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 const int c_last = cta_of_unit(tg_u0 + p.nblocks - 1, p.U, p.P);
                 if (ticket == static_cast<uint32_t>(c_last - c_first)) {
                     __threadfence();
-                    // the 32 lanes share the R*MM*4 sums of the tile
-                    for (int e = lane; e < R * MM * 4; e += 32) {
+                    // Every CTA after c_first starts inside this tile-group, so
+                    // this tile-group is its first (slot 0); c_first used slot 1
+                    // unless its range also starts at the tile-group's first unit.
+                    const long long cf_u0 = static_cast<long long>(c_first) * p.U / p.P;
+                    const int cf_slot = (cf_u0 < tg_u0) ? 1 : 0;
+                    constexpr int E = R * MM * 4;
+                    // the 32 lanes share the E sums of the tile; partials are
+                    // loaded 8 CTAs at a time and added in CTA order
+                    for (int e = lane; e < E; e += 32) {
                         float sum = 0.0f;
-                        for (int cc = c_first; cc <= c_last; ++cc) {
-                            const long long cc_u0 = static_cast<long long>(cc) * p.U / p.P;
-                            const int cc_slot = (tg == static_cast<int>(cc_u0 / p.nblocks)) ? 0 : 1;
-                            const float* src = p.partials +
-                                ((static_cast<size_t>(cc) * 2 + cc_slot) * WARPS + warp) * (R * MM * 4);
-                            sum = __fadd_rn(sum, __ldcg(src + e));
+                        for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
+                            float part[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int cc = cc0 + i;
+                                part[i] = 0.0f;
+                                if (cc <= c_last) {
+                                    const int cs = (cc == c_first) ? cf_slot : 0;
+                                    part[i] = __ldcg(p.partials +
+                                                     ((static_cast<size_t>(cc) * 2 + cs) * WARPS + warp) * E + e);
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                if (cc0 + i <= c_last) sum = __fadd_rn(sum, part[i]);
                         }
                         const int q = e & 3, rm = e >> 2;
                         const int r = rm / MM, m = rm - r * MM;
