@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 
 HEADLINE = "gemm_m8_k5120_n17408_k3"
 METRIC = "trellis GEMM packed-weight GB/s"
+METRIC_DECODE = "trellis decode packed-weight GB/s"
 DECODE_OPS_PER_WEIGHT = 10        # algorithmic integer/fp32 ops per decoded weight
 ALU_LANES_PER_SM = 128            # 4 sub-partitions x 32 lanes, one op per lane per clock
 
@@ -208,19 +209,28 @@ def run_ours(args, wl):
     dx = to_dev(x, torch, "bf16")
     dscales = to_dev(scales, torch, "bf16")
     dcodes = [to_dev(codes, torch, "u32") for _ in range(n_rot)]
-    out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
-    ws_bytes = binding.gemm_workspace_bytes(wl.M, wl.K, wl.N, wl.k)
-    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
     s_handle = stream.cuda_stream
-    torch.cuda.synchronize()
+    if args.entry == "gemm":
+        out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+        ws_bytes = binding.gemm_workspace_bytes(wl.M, wl.K, wl.N, wl.k)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
 
-    def call(i):
-        rc = lib.trellis_gemm_ws(dx.data_ptr(), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
-                                 wl.M, wl.K, wl.N, wl.k, wl.L, wl.T, out.data_ptr(),
-                                 ws.data_ptr(), ws.numel(), s_handle)
-        if rc != 0:
-            raise RuntimeError(f"trellis_gemm_ws failed: {binding.status_string(rc)}")
+        def call(i):
+            rc = lib.trellis_gemm_ws(dx.data_ptr(), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
+                                     wl.M, wl.K, wl.N, wl.k, wl.L, wl.T, out.data_ptr(),
+                                     ws.data_ptr(), ws.numel(), s_handle)
+            if rc != 0:
+                raise RuntimeError(f"trellis_gemm_ws failed: {binding.status_string(rc)}")
+    else:
+        wout = torch.empty((wl.N, wl.K), dtype=torch.bfloat16, device="cuda")
+
+        def call(i):
+            rc = lib.trellis_decode(dcodes[i % n_rot].data_ptr(), dscales.data_ptr(), wl.K, wl.N, wl.k,
+                                    wl.L, wl.T, wout.data_ptr(), s_handle)
+            if rc != 0:
+                raise RuntimeError(f"trellis_decode failed: {binding.status_string(rc)}")
+    torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -269,11 +279,18 @@ def run_ours(args, wl):
         ds2 = torch.empty_like(dscales)
         n_e2e = max(3, min(args.steps, args.e2e_steps))
 
+        if args.entry == "decode":
+            from trellis_quantized_weight_gb300 import decode as tq_decode
+            hout = torch.empty((wl.N, wl.K), dtype=torch.bfloat16).pin_memory()
+
         def e2e_step():
-            dx2.copy_(hx, non_blocking=True)
             dc2.copy_(hc, non_blocking=True)
             ds2.copy_(hs, non_blocking=True)
-            y = tq_gemm(dx2, dc2, ds2, wl.k)
+            if args.entry == "gemm":
+                dx2.copy_(hx, non_blocking=True)
+                y = tq_gemm(dx2, dc2, ds2, wl.k)
+            else:
+                y = tq_decode(dc2, ds2, wl.K, wl.k)
             hout.copy_(y, non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -295,35 +312,43 @@ def run_ours(args, wl):
             t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t[0])
-        h2d = hx.numel() * 2 + hc.numel() * 4 + hs.numel() * 2
+        h2d = (hx.numel() * 2 if args.entry == "gemm" else 0) + hc.numel() * 4 + hs.numel() * 2
         e2e = {"value": round(world * wl.code_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_call": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": hout.numel() * 2}
 
-    # ---- roofline of the fused kernel (the only kernel of the step) ----
+    # ---- roofline of the step's only kernel ----
     peaks, peak_src = measured_peaks()
     sm_max = float(peaks.get("sm_max_mhz") or 2070.0)
+    hbm_peak = float(peaks["hbm_gbs"])
     alu_peak = props.multi_processor_count * ALU_LANES_PER_SM * sm_max * 1e6 / 1e12   # Tops/s
-    ops = wl.weights * (DECODE_OPS_PER_WEIGHT + wl.M)
-    hbm_bytes = wl.code_bytes + wl.M * wl.K * 2 + wl.M * wl.N * 2
     t_kernel = kernel_ms * 1e-3
+    if args.entry == "gemm":
+        ops = wl.weights * (DECODE_OPS_PER_WEIGHT + wl.M)
+        hbm_bytes = wl.code_bytes + wl.M * wl.K * 2 + wl.M * wl.N * 2
+        kernel_name = "gemm_smallm"
+    else:
+        ops = wl.weights * DECODE_OPS_PER_WEIGHT
+        hbm_bytes = wl.code_bytes + wl.weights * 2
+        kernel_name = "decode"
     alu_achieved = ops / t_kernel / 1e12
     hbm_achieved = hbm_bytes / t_kernel / 1e9
     t_roof_alu = ops / (alu_peak * 1e12)
-    t_roof_hbm = hbm_bytes / (float(peaks["hbm_gbs"]) * 1e9)
+    t_roof_hbm = hbm_bytes / (hbm_peak * 1e9)
     bound = "alu" if t_roof_alu >= t_roof_hbm else "hbm"
     roof = {"bound": bound,
             "achieved": round(alu_achieved if bound == "alu" else hbm_achieved, 3),
-            "peak": round(alu_peak if bound == "alu" else float(peaks["hbm_gbs"]), 3),
+            "peak": round(alu_peak if bound == "alu" else hbm_peak, 3),
             "unit": "Tops/s" if bound == "alu" else "GB/s",
-            "frac": round((alu_achieved / alu_peak) if bound == "alu" else
-                          (hbm_achieved / float(peaks["hbm_gbs"])), 4),
-            "traffic": profiled_traffic("gemm_smallm", wl.name),
+            "frac": round((alu_achieved / alu_peak) if bound == "alu" else (hbm_achieved / hbm_peak), 4),
+            "traffic": profiled_traffic(kernel_name, wl.name),
             "peak_source": (f"{peak_src}: {props.multi_processor_count} SMs x {ALU_LANES_PER_SM} lanes x "
-                            f"{sm_max:.0f} MHz" if bound == "alu" else f"{peak_src} hbm_gbs"),
+                            f"{sm_max:.0f} MHz (of measured max clock)" if bound == "alu"
+                            else f"{peak_src} hbm_gbs (of measured)"),
             "ops_per_launch": ops, "algorithmic_bytes_per_launch": hbm_bytes,
             "hbm_GBps": round(hbm_achieved, 1),
-            "hbm_frac": round(hbm_achieved / float(peaks["hbm_gbs"]), 4),
+            "hbm_frac": round(hbm_achieved / hbm_peak, 4),
+            "alu_frac": round(alu_achieved / alu_peak, 4),
             "roofline_us": round(max(t_roof_alu, t_roof_hbm) * 1e6, 2),
             "kernel_us": round(kernel_ms * 1e3, 2)}
 
@@ -336,12 +361,13 @@ def run_ours(args, wl):
 
     value = world * wl.code_bytes / (ms_step * 1e-3) / 1e9
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC if args.entry == "gemm" else METRIC_DECODE, "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "k": wl.k, "L": wl.L,
-                   "T": wl.T, "parallelism": f"replicas{world}",
+        "config": {"workload": wl.name, "entry": "trellis_" + args.entry, "M": wl.M, "K": wl.K, "N": wl.N,
+                   "k": wl.k, "L": wl.L, "T": wl.T, "parallelism": f"replicas{world}",
                    "l2": f"rotating {n_rot} code copies ({n_rot * wl.code_bytes / 1e6:.0f} MB > 2x L2)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
         "clocks": clocks, "host_wall_s": round(t_host, 3),
@@ -410,6 +436,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--entry", choices=["gemm", "decode"], default="gemm",
+                    help="time the fused product (default) or the dense decode")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
