@@ -27,8 +27,9 @@
  * float(w)*float(x) in fp32 and rounds each output once to bf16 (nearest even).
  *
  * Accepted geometry: k in {2, 3, 4}, L == 12, T == 256, K a positive multiple
- * of T, N >= 1, and for trellis_gemm 1 <= M <= 16.  Anything else returns
- * TRELLIS_ERR_UNSUPPORTED or TRELLIS_ERR_SHAPE before any launch.
+ * of T, N >= 1, and for trellis_gemm 1 <= M <= 16 (CUDA cores) or M == 64
+ * (tensor cores).  Anything else returns TRELLIS_ERR_UNSUPPORTED or
+ * TRELLIS_ERR_SHAPE before any launch.
  *
  * Every call is asynchronous on `stream` (0 = the legacy default stream): it
  * validates its arguments on the host, enqueues its kernels and returns
@@ -101,7 +102,11 @@ int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, 
  *   codes   device, uint32 [N, K*k/32], 16-byte aligned.
  *   scales  device, bf16 [N].
  *   out     device, bf16 [M, N]; fully overwritten.
- *   1 <= M <= 16.
+ *   1 <= M <= 16, or M == 64.
+ *
+ * For M == 64 the decoded bf16 weight tiles are multiplied on the tensor
+ * cores (tcgen05, fp32 accumulation in tensor memory); that path needs no
+ * workspace and its waits are bounded (see trellis_device_status).
  *
  * The summation order is fixed by the launch geometry, so repeated calls on
  * the same device give identical bits.  The kernel balances work across all
@@ -111,7 +116,8 @@ int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, 
  * later calls reuse it, so that first call must not happen during stream
  * capture, and calls that use it must not overlap on the GPU (use
  * trellis_gemm_ws with separate workspaces for concurrent streams).
- * Errors: as trellis_decode, plus M outside 1..16 -> TRELLIS_ERR_UNSUPPORTED.
+ * Errors: as trellis_decode, plus M outside 1..16 and not 64 ->
+ * TRELLIS_ERR_UNSUPPORTED.
  */
 int trellis_gemm(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M, int K,
                  int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
@@ -144,6 +150,15 @@ int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t
 int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
                     int K, int N, int k, int L, int T, uint16_t *out, void *workspace,
                     size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * trellis_device_status — synchronise `stream`, then report whether a bounded
+ * device-side wait of the tensor-core product gave up since the last query
+ * (TRELLIS_ERR_TIMEOUT; the affected outputs are undefined) or not
+ * (TRELLIS_OK).  Clears the flag.  No counterpart on the pages: it is how the
+ * library surfaces its own wait limits.
+ */
+int trellis_device_status(cudaStream_t stream);
 
 /*
  * trellis_gemm_noalloc — trellis_gemm for callers that cannot allocate device

@@ -66,7 +66,8 @@ def test_decode_rejects(lib, args, want):
 
 
 @pytest.mark.parametrize("M,K,N,k,L,T,want", [
-    (0, 5120, 64, 4, 12, 256, -3), (17, 5120, 64, 4, 12, 256, -3), (64, 5120, 64, 4, 12, 256, -3),
+    (0, 5120, 64, 4, 12, 256, -3), (17, 5120, 64, 4, 12, 256, -3), (65, 5120, 64, 4, 12, 256, -3),
+    (32, 5120, 64, 4, 12, 256, -3), (63, 5120, 64, 4, 12, 256, -3),
     (5, 5120, 64, 6, 12, 256, -3), (5, 5000, 64, 4, 12, 256, -2), (5, 5120, 0, 4, 12, 256, -2),
 ])
 def test_gemm_rejects(lib, M, K, N, k, L, T, want):
@@ -74,6 +75,17 @@ def test_gemm_rejects(lib, M, K, N, k, L, T, want):
     assert lib.trellis_gemm_ws(FAKE, FAKE, FAKE, M, K, N, k, L, T, FAKE, FAKE, 1 << 20, None) == want
     n = ctypes.c_size_t(0)
     assert lib.trellis_gemm_workspace_size(M, K, N, k, L, T, ctypes.byref(n)) == want
+
+
+def test_m64_needs_no_workspace_and_checks_pointers(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.trellis_gemm_workspace_size(64, 5120, 17408, 4, 12, 256, ctypes.byref(n)) == 0
+    assert n.value == 0
+    # rejected before any launch: NULL / misaligned pointers, bad geometry
+    assert lib.trellis_gemm(0, FAKE, FAKE, 64, 5120, 64, 4, 12, 256, FAKE, None) == -1
+    assert lib.trellis_gemm(FAKE + 2, FAKE, FAKE, 64, 5120, 64, 4, 12, 256, FAKE, None) == -4
+    assert lib.trellis_gemm(FAKE, FAKE, FAKE, 64, 5000, 64, 4, 12, 256, FAKE, None) == -2
+    assert lib.trellis_gemm(FAKE, FAKE, FAKE, 64, 5120, 64, 5, 12, 256, FAKE, None) == -3
 
 
 def test_gemm_rejects_pointers(lib):

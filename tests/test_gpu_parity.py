@@ -90,6 +90,34 @@ def test_gemm_shapes(tq, oracle_lib, M, K, N, k):
     assert_gemm_close(got, ref, refabs, f"M={M} K={K} N={N} k={k}")
 
 
+@pytest.mark.parametrize("k", [2, 3, 4])
+@pytest.mark.parametrize("N,K", [(128, 256), (300, 512), (1000, 1024), (129, 256 * 9)])
+def test_gemm_m64_tensor_cores(tq, oracle_lib, k, N, K):
+    """M = 64 runs on tcgen05 (decoded bf16 tiles, fp32 accumulation in tensor memory)."""
+    from trellis_quantized_weight_gb300 import binding
+    M = 64
+    x, codes, scales = _inputs(M, K, N, k, seed=640 + 7 * k + N + K)
+    got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), k))
+    assert binding.load().trellis_device_status(None) == 0
+    w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+    ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+    assert_gemm_close(got, ref, refabs, f"M=64 N={N} K={K} k={k}")
+
+
+def test_gemm_m64_one_hot_is_exact(tq, oracle_lib):
+    """Each of the 64 rows of x selects a different weight column, bit for bit."""
+    N, K, k = 256, 1024, 4
+    _, codes, scales = _inputs(1, K, N, k, seed=641)
+    w = oracle_lib.decode(codes, scales, K, N, k)
+    cols = [(37 * i + 5) % K for i in range(64)]
+    e = np.zeros((64, K), np.uint16)
+    for i, j in enumerate(cols):
+        e[i, j] = 0x3F80
+    got = host_bits(tq.gemm(dev_bf16(e), dev_codes(codes), dev_bf16(scales), k))
+    for i, j in enumerate(cols):
+        assert np.array_equal(got[i], w[:, j]), i
+
+
 def test_gemm_one_hot_is_exact(tq, oracle_lib):
     """x = e_j picks column j of the decoded weights, bit for bit."""
     N, K, k = 700, 1280, 3
@@ -172,9 +200,8 @@ def test_gemm_workspace_errors(tq):
 
 
 # ----------------------------------------------- full-size quantised-linear --
-WORKLOADS_SMALL_M = ["gemm_m5_k5120_n17408_k2", "gemm_m8_k5120_n17408_k3",
-                     "gemm_m15_k5120_n17408_k4", "gemv_m1_k17408_n5120_k4"]
-ALL_WORKLOADS = WORKLOADS_SMALL_M + ["prefill_m64_k5120_n17408_k4"]
+ALL_WORKLOADS = ["gemm_m5_k5120_n17408_k2", "gemm_m8_k5120_n17408_k3", "gemm_m15_k5120_n17408_k4",
+                 "gemv_m1_k17408_n5120_k4", "prefill_m64_k5120_n17408_k4"]
 
 
 @pytest.fixture(scope="module")
@@ -199,7 +226,7 @@ def test_full_decode_bitexact(tq, oracle_lib, full_inputs, name):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("name", WORKLOADS_SMALL_M)
+@pytest.mark.parametrize("name", ALL_WORKLOADS)
 def test_full_gemm(tq, oracle_lib, full_inputs, name):
     wl, x, codes, scales = full_inputs(name)
     got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), wl.k))

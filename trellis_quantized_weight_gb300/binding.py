@@ -33,6 +33,7 @@ SIGNATURES = {
     "trellis_gemm_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "trellis_gemm_ws": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "trellis_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "trellis_device_status": (_I, [_P]),
 }
 
 
@@ -171,7 +172,7 @@ def gemm(x, codes, scales, k: int, L: int = 12, T: int = 256, out=None, stream=N
     if tuple(out.shape) != (M, N):
         raise ValueError("out must be [M, N]")
     nbytes = gemm_workspace_bytes(M, K, N, k, L, T)
-    ws = _workspace(x.device, nbytes)
+    ws = _workspace(x.device, max(nbytes, 256))
     rc = abi_gemm_ws(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, K, N, k, L, T,
                      out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(x.device, stream))
     _check(rc, "trellis_gemm_ws")

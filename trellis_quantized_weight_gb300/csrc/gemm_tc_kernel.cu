@@ -1,0 +1,403 @@
+// Fused decode-and-multiply for M = 64 activation rows on the 5th-generation
+// tensor cores (tcgen05, sm_103a).
+//
+// What it computes is the same as the CUDA-core product (the wide-prefill
+// kernel on the page "mlx-bun 0.2.0 -> 0.4.0", trellis-wide-prefill.ts):
+// out[m, n] = bf16( sum_k w[n, k] * x[m, k] ) with w the decoded bf16 weights.
+// At M = 64 the multiply is a real dense contraction, so the decoded weights
+// go to the tensor cores instead of the FMA pipes:
+//
+//   D[n, m] (TMEM, fp32, 128 lanes x 64 columns) += A[n, k] * B[m, k]^T
+//   A = decoded weight tile, 128 rows x 16 k, bf16, K-major, shared memory
+//   B = activation tile,      64 rows x 16 k, bf16, K-major, shared memory
+//
+// One CTA owns 128 weight rows and the whole K range.  Its warps:
+//   * 16 decode warps write the bf16 weights of one 128-k stage into shared
+//     memory in the canonical K-major layout (8-row x 16-byte core matrices,
+//     no swizzle); lanes of one shared-memory phase write 8 different rows,
+//     so the stores are conflict-free.  The quotient is looked up in a
+//     per-lane shared-memory table (conflict-free, see trellis_device.cuh).
+//   * 1 TMA warp loads the activation tile of the stage with 3-D tensor copies
+//     that land directly in the same core-matrix layout.
+//   * 1 MMA warp: one thread issues the 8 tcgen05.mma (K = 16 each) of a stage
+//     and commits them to the stage's "empty" barrier.
+// Two stages are in flight (mbarrier full/empty pairs).  After the last stage
+// the decode warps read the accumulator back with tcgen05.ld, round to bf16
+// and store out[m, n] (each store instruction writes 32 consecutive n).
+//
+// Every mbarrier wait is bounded; a wait that runs out records an error in a
+// device word (read by trellis_device_status) and the CTA winds down.
+#include <cuda.h>
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+#include "trellis_device.cuh"
+
+namespace trellis {
+
+__device__ unsigned int g_tc_error = 0u;
+
+namespace {
+
+constexpr int kTcRows = 128;                 // weight rows per CTA (MMA M)
+constexpr int kTcM = 64;                     // activation rows (MMA N)
+constexpr int kTcStageK = 128;               // k per pipeline stage
+constexpr int kTcStages = 2;
+constexpr int kTcDecodeWarps = 16;
+constexpr int kTcThreads = (kTcDecodeWarps + 2) * 32;
+constexpr int kTcTmaWarp = kTcDecodeWarps;
+constexpr int kTcMmaWarp = kTcDecodeWarps + 1;
+constexpr int kTcTmemCols = 64;
+
+// Over all 4096 windows of 12 bits the byte sum S of the hash spans [62, 964]
+// (codes -448 .. 454), so the table keeps only those 903 entries.
+constexpr int kSumLo = 62;
+constexpr int kSumHi = 964;
+constexpr int kTableEntries = kSumHi - kSumLo + 1;
+constexpr int kTableBytes = kTableEntries * 32 * 4;                  // 115,584
+constexpr int kTableRegion = (kTableBytes + 1023) / 1024 * 1024;     // 116,736
+
+constexpr int kABytes = kTcRows * kTcStageK * 2;     // 32 KB
+constexpr int kBBytes = kTcM * kTcStageK * 2;        // 16 KB
+constexpr int kCoreSBO = (kTcStageK / 8) * 128;      // bytes between 8-row groups: 2 KB
+constexpr int kCoreLBO = 128;                        // bytes between k-adjacent core matrices
+
+constexpr int kOffA = kTableRegion;
+constexpr int kOffB = kOffA + kTcStages * kABytes;
+constexpr int kOffBar = kOffB + kTcStages * kBBytes;
+constexpr int kBarFull = 0, kBarEmpty = kTcStages, kBarDone = 2 * kTcStages;
+constexpr int kOffTaddr = kOffBar + (2 * kTcStages + 1) * 8;
+constexpr int kTcSmemBytes = kOffTaddr + 16;
+
+constexpr uint32_t kWaitLimit = 1u << 24;   // polls before a wait gives up
+
+// ---- PTX wrappers ------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 " selp.b32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0u;
+}
+// Bounded wait: false (and the error word set) when it runs out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicOr(&g_tc_error, 1u);
+    return false;
+}
+__device__ __forceinline__ void fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+// Shared-memory matrix descriptor: no swizzle, K-major core matrices.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>(kCoreLBO >> 4) << 16) |
+           (static_cast<uint64_t>(kCoreSBO >> 4) << 32) |
+           (1ull << 46);                       // descriptor version for tcgen05
+}
+// Instruction descriptor: kind::f16, D fp32, A and B bf16, both K-major,
+// N = 64, M = 128.
+constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                (static_cast<uint32_t>(kTcM >> 3) << 17) |
+                                (static_cast<uint32_t>(kTcRows >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(kInstrDesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ float tc_quotient(uint32_t win, uint32_t lane_base) {
+    const uint32_t z = win * kHashMul + kHashAdd;
+    const uint32_t addr = __dp4a(z, 0x80808080u, lane_base);
+    float v;
+    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+template <int KB>
+__device__ __forceinline__ void tc_load_group(const uint32_t* __restrict__ row_codes, bool ok, int stage,
+                                              int gi, uint32_t (&w)[KB], uint32_t& extra) {
+    constexpr int WPB = kGroupsPerBlock * KB;
+    const int b = stage >> 1, g = 4 * (stage & 1) + gi;
+    if (ok) {
+        const uint32_t* p = row_codes + b * WPB + (kGroupsPerBlock - 1 - g) * KB;
+        if constexpr (KB == 4) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        } else if constexpr (KB == 2) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+            w[0] = v.x; w[1] = v.y;
+        } else {
+#pragma unroll
+            for (int i = 0; i < KB; ++i) w[i] = __ldg(p + i);
+        }
+        // groups 0 and 4 take their lookahead word from the other half block
+        extra = (gi == 0) ? __ldg(row_codes + b * WPB + ((kGroupsPerBlock - g) * KB) % WPB) : 0u;
+    } else {
+#pragma unroll
+        for (int i = 0; i < KB; ++i) w[i] = 0u;
+        extra = 0u;
+    }
+}
+
+template <int KB>
+__global__ void __launch_bounds__(kTcThreads, 1)
+gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+               uint16_t* __restrict__ out, int K, int N, int row_words,
+               const __grid_constant__ CUtensorMap x_map) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const uint32_t bar_full = sbase + kOffBar + 8 * kBarFull;
+    const uint32_t bar_empty = sbase + kOffBar + 8 * kBarEmpty;
+    const uint32_t bar_done = sbase + kOffBar + 8 * kBarDone;
+    const int nstages = K / kTcStageK;
+    const int n0 = blockIdx.x * kTcRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(bar_full + 8 * s, kTcDecodeWarps + 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_shared();
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(sbase + kOffTaddr), "r"(kTcTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp < kTcDecodeWarps) {
+        // quotient table for S in [62, 964], one copy per lane
+        float* table = reinterpret_cast<float*>(smem);
+        for (int e = threadIdx.x; e < kTableEntries * 8; e += kTcDecodeWarps * 32) {
+            const int si = e >> 3, quad = e & 7;
+            const float v = code_to_value(static_cast<float>(si + kSumLo - 510));
+            *reinterpret_cast<float4*>(table + si * 32 + quad * 4) = make_float4(v, v, v, v);
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t taddr = *reinterpret_cast<volatile uint32_t*>(smem + kOffTaddr);
+
+    if (warp < kTcDecodeWarps) {
+        // ---------------------------------------------------------------- decode
+        const int row_local = warp * 8 + (lane & 7);
+        const int gi = (lane >> 3) & 3;
+        const int row = n0 + row_local;
+        const bool ok = row < N;
+        const float sr = ok ? bf16_bits_to_f32(__ldg(scales + row)) : 0.0f;
+        const float2 s2 = make_float2(sr, sr);
+        const uint32_t* row_codes = codes + static_cast<size_t>(ok ? row : 0) * row_words;
+        const uint32_t lane_tbl = sbase + 4u * static_cast<uint32_t>(lane) - static_cast<uint32_t>(kSumLo * 128);
+        const int src_lane = (gi == 0) ? lane : lane - 8;
+        // this thread's 4 core-matrix rows inside a stage's A tile
+        const uint32_t a_row_off = static_cast<uint32_t>((row_local >> 3) * kCoreSBO + gi * 4 * kCoreLBO +
+                                                         (row_local & 7) * 16);
+        uint32_t cw[KB], cx;
+        tc_load_group<KB>(row_codes, ok, 0, gi, cw, cx);
+        bool alive = true;
+        for (int i = 0; i < nstages && alive; ++i) {
+            const int s = i & 1;
+            uint32_t nw[KB], nx = 0u;
+            if (i + 1 < nstages) {
+                tc_load_group<KB>(row_codes, ok, i + 1, gi, nw, nx);
+            } else {
+#pragma unroll
+                for (int q = 0; q < KB; ++q) nw[q] = 0u;
+            }
+            uint32_t w[KB + 1];
+#pragma unroll
+            for (int q = 0; q < KB; ++q) w[q] = cw[q];
+            const uint32_t nb = __shfl_sync(0xffffffffu, cw[0], src_lane);
+            w[KB] = (gi == 0) ? cx : nb;
+
+            uint32_t packed[16];
+#pragma unroll
+            for (int jp = 0; jp < 16; ++jp) {
+                const float2 v = make_float2(tc_quotient(group_window<KB>(w, 2 * jp), lane_tbl),
+                                             tc_quotient(group_window<KB>(w, 2 * jp + 1), lane_tbl));
+                const float2 ws = __fmul2_rn(v, s2);
+                packed[jp] = pack_bf16x2(ws.x, ws.y);
+            }
+            if (i >= kTcStages) alive = mbar_wait(bar_empty + 8 * s, ((i >> 1) + 1) & 1);
+            if (!alive) break;
+            const uint32_t dst = sbase + kOffA + s * kABytes + a_row_off;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                             :: "r"(dst + q * kCoreLBO), "r"(packed[4 * q]), "r"(packed[4 * q + 1]),
+                                "r"(packed[4 * q + 2]), "r"(packed[4 * q + 3]) : "memory");
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_full + 8 * s);
+#pragma unroll
+            for (int q = 0; q < KB; ++q) cw[q] = nw[q];
+            cx = nx;
+        }
+
+        // -------------------------------------------------------------- epilogue
+        const bool done = alive && mbar_wait(bar_done, 0);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (done) {
+            const int sub = warp & 3, colq = warp >> 2;
+            uint32_t r[16];
+            const uint32_t ta = taddr + (static_cast<uint32_t>(32 * sub) << 16) + static_cast<uint32_t>(16 * colq);
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                "%12, %13, %14, %15}, [%16];"
+                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                  "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                  "=r"(r[14]), "=r"(r[15])
+                : "r"(ta));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            const int n = n0 + 32 * sub + lane;
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    out[static_cast<size_t>(16 * colq + j) * N + n] = bf16_bits_rn(__uint_as_float(r[j]));
+            }
+        }
+    } else if (warp == kTcTmaWarp) {
+        // ------------------------------------------------------------- x via TMA
+        if (lane == 0) {
+            for (int i = 0; i < nstages; ++i) {
+                const int s = i & 1;
+                if (i >= kTcStages && !mbar_wait(bar_empty + 8 * s, ((i >> 1) + 1) & 1)) break;
+                mbar_arrive_expect_tx(bar_full + 8 * s, kBBytes);
+                const uint32_t dst = sbase + kOffB + s * kBBytes;
+#pragma unroll
+                for (int mg = 0; mg < kTcM / 8; ++mg)
+                    tma_load_3d(dst + mg * kCoreSBO, &x_map, 0, 8 * mg, i * (kTcStageK / 8), bar_full + 8 * s);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            bool ok = true;
+            for (int i = 0; i < nstages; ++i) {
+                const int s = i & 1;
+                if (!mbar_wait(bar_full + 8 * s, (i >> 1) & 1)) { ok = false; break; }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t a0 = sbase + kOffA + s * kABytes;
+                const uint32_t b0 = sbase + kOffB + s * kBBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTcStageK / 16; ++kk)
+                    mma_bf16(taddr, smem_desc(a0 + kk * 2 * kCoreLBO), smem_desc(b0 + kk * 2 * kCoreLBO),
+                             (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar_empty + 8 * s);
+            }
+            mma_commit(bar_done);   // tracks every MMA issued above
+            (void)ok;
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(kTcTmemCols)
+                     : "memory");
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// x [64, K] bf16 row-major seen as a 3-D tensor (8 k, m, K/8): a box of
+// (8, 8, 16) is one 8-row group of 16 k-adjacent core matrices, laid out in
+// shared memory exactly as the MMA's K-major no-swizzle operand.
+bool make_x_map(CUtensorMap* map, const uint16_t* x, int K) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(kTcM), static_cast<cuuint64_t>(K / 8)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 16};
+    const cuuint32_t box[3] = {8, 8, kTcStageK / 8};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KB>
+int launch_tc_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K, int N,
+                       uint16_t* out, cudaStream_t stream) {
+    CUtensorMap map;
+    if (!make_x_map(&map, x, K)) return -5;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemm_tc_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes) !=
+            cudaSuccess)
+            return -5;
+        attr_set = true;
+    }
+    const int grid = (N + kTcRows - 1) / kTcRows;
+    gemm_tc_kernel<KB><<<grid, kTcThreads, kTcSmemBytes, stream>>>(codes, scales, out, K, N, K / 32 * KB, map);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+}  // namespace
+
+int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
+                   uint16_t* out, cudaStream_t stream) {
+    switch (k) {
+        case 2: return launch_tc_instance<2>(x, codes, scales, K, N, out, stream);
+        case 3: return launch_tc_instance<3>(x, codes, scales, K, N, out, stream);
+        case 4: return launch_tc_instance<4>(x, codes, scales, K, N, out, stream);
+        default: return -3;
+    }
+}
+
+int tc_take_device_error(unsigned int* flags) {
+    unsigned int v = 0u;
+    if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v)) != cudaSuccess) return -5;
+    if (v != 0u) {
+        const unsigned int zero = 0u;
+        if (cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(zero)) != cudaSuccess) return -5;
+    }
+    *flags = v;
+    return 0;
+}
+
+}  // namespace trellis

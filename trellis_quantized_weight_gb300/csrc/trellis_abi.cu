@@ -49,6 +49,10 @@ int check_geometry(int K, int N, int k, int L, int T) {
     return TRELLIS_OK;
 }
 
+// 1 <= M <= 16 runs on the CUDA cores; M == 64 on the tensor cores.
+constexpr int kTensorCoreM = 64;
+bool gemm_m_supported(int M) { return (M >= 1 && M <= 16) || M == kTensorCoreM; }
+
 int check_codes(const uint32_t* codes, const uint16_t* scales) {
     if (codes == nullptr || scales == nullptr) return TRELLIS_ERR_NULL;
     if (!aligned(codes, 16) || !aligned(scales, 2)) return TRELLIS_ERR_ALIGN;
@@ -62,7 +66,7 @@ int check_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales,
     if (rc != TRELLIS_OK) return rc;
     rc = check_geometry(K, N, k, L, T);
     if (rc != TRELLIS_OK) return rc;
-    if (M < 1 || M > 16) return TRELLIS_ERR_UNSUPPORTED;
+    if (!gemm_m_supported(M)) return TRELLIS_ERR_UNSUPPORTED;
     if (!aligned(x, 16) || !aligned(out, 2)) return TRELLIS_ERR_ALIGN;
     return TRELLIS_OK;
 }
@@ -137,7 +141,11 @@ int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t
     if (bytes == nullptr) return TRELLIS_ERR_NULL;
     int rc = check_geometry(K, N, k, L, T);
     if (rc != TRELLIS_OK) return rc;
-    if (M < 1 || M > 16) return TRELLIS_ERR_UNSUPPORTED;
+    if (!gemm_m_supported(M)) return TRELLIS_ERR_UNSUPPORTED;
+    if (M == kTensorCoreM) {   // the tensor-core path needs no workspace
+        *bytes = 0;
+        return TRELLIS_OK;
+    }
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
@@ -150,6 +158,7 @@ int trellis_gemm_ws(const uint16_t* x, const uint32_t* codes, const uint16_t* sc
                     cudaStream_t stream) {
     int rc = check_gemm(x, codes, scales, M, K, N, k, L, T, out);
     if (rc != TRELLIS_OK) return rc;
+    if (M == kTensorCoreM) return trellis::launch_gemm_tc(x, codes, scales, K, N, k, out, stream);
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
@@ -165,6 +174,7 @@ int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scale
                  int k, int L, int T, uint16_t* out, cudaStream_t stream) {
     int rc = check_gemm(x, codes, scales, M, K, N, k, L, T, out);
     if (rc != TRELLIS_OK) return rc;
+    if (M == kTensorCoreM) return trellis::launch_gemm_tc(x, codes, scales, K, N, k, out, stream);
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
@@ -174,6 +184,13 @@ int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scale
     rc = owned_workspace(dev, need, &ws);
     if (rc != TRELLIS_OK) return rc;
     return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, ws, need, stream, dev);
+}
+
+int trellis_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return TRELLIS_ERR_CUDA;
+    unsigned int flags = 0u;
+    if (trellis::tc_take_device_error(&flags) != 0) return TRELLIS_ERR_CUDA;
+    return flags != 0u ? TRELLIS_ERR_TIMEOUT : TRELLIS_OK;
 }
 
 }  // extern "C"
