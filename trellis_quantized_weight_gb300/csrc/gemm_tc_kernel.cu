@@ -21,7 +21,7 @@
 //     that land directly in the same core-matrix layout.
 //   * 1 MMA warp: one thread issues the 8 tcgen05.mma (K = 16 each) of a stage
 //     and commits them to the stage's "empty" barrier.
-// Two stages are in flight (mbarrier full/empty pairs).  After the last stage
+// Four stages are in flight (mbarrier full/empty pairs).  After the last stage
 // the decode warps read the accumulator back with tcgen05.ld, round to bf16
 // and store out[m, n] (each store instruction writes 32 consecutive n).
 //
@@ -43,7 +43,7 @@ namespace {
 constexpr int kTcRows = 128;                 // weight rows per CTA (MMA M)
 constexpr int kTcM = 64;                     // activation rows (MMA N)
 constexpr int kTcStageK = 128;               // k per pipeline stage
-constexpr int kTcStages = 2;
+constexpr int kTcStages = 4;
 constexpr int kTcDecodeWarps = 16;
 constexpr int kTcThreads = (kTcDecodeWarps + 2) * 32;
 constexpr int kTcTmaWarp = kTcDecodeWarps;
@@ -56,7 +56,13 @@ constexpr int kSumLo = 62;
 constexpr int kSumHi = 964;
 constexpr int kTableEntries = kSumHi - kSumLo + 1;
 constexpr int kTableBytes = kTableEntries * 32 * 4;                  // 115,584
-constexpr int kTableRegion = (kTableBytes + 1023) / 1024 * 1024;     // 116,736
+// Quotient by the per-lane table (one shared load) or by the three-op
+// residual correction (ALU only).  This kernel's shared-memory pipe is busy
+// with the A tiles, the activation tiles and the tensor cores' operand reads,
+// while its issue slots are not, so the ALU form is used and the table's
+// shared memory goes to deeper pipelining instead.
+constexpr bool kTcLut = false;
+constexpr int kTableRegion = kTcLut ? (kTableBytes + 1023) / 1024 * 1024 : 0;
 
 constexpr int kABytes = kTcRows * kTcStageK * 2;     // 32 KB
 constexpr int kBBytes = kTcM * kTcStageK * 2;        // 16 KB
@@ -71,6 +77,8 @@ constexpr int kOffTaddr = kOffBar + (2 * kTcStages + 1) * 8;
 constexpr int kTcSmemBytes = kOffTaddr + 16;
 
 constexpr uint32_t kWaitLimit = 1u << 24;   // polls before a wait gives up
+
+
 
 // ---- PTX wrappers ------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -192,7 +200,7 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                      :: "r"(sbase + kOffTaddr), "r"(kTcTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp < kTcDecodeWarps) {
+    if (kTcLut && warp < kTcDecodeWarps) {
         // quotient table for S in [62, 964], one copy per lane
         float* table = reinterpret_cast<float*>(smem);
         for (int e = threadIdx.x; e < kTableEntries * 8; e += kTcDecodeWarps * 32) {
@@ -220,46 +228,64 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         // this thread's 4 core-matrix rows inside a stage's A tile
         const uint32_t a_row_off = static_cast<uint32_t>((row_local >> 3) * kCoreSBO + gi * 4 * kCoreLBO +
                                                          (row_local & 7) * 16);
-        uint32_t cw[KB], cx;
-        tc_load_group<KB>(row_codes, ok, 0, gi, cw, cx);
-        bool alive = true;
-        for (int i = 0; i < nstages && alive; ++i) {
-            const int s = i & 1;
-            uint32_t nw[KB], nx = 0u;
-            if (i + 1 < nstages) {
-                tc_load_group<KB>(row_codes, ok, i + 1, gi, nw, nx);
+        // code words travel through a 4-deep register ring: stage i+3 is
+        // loaded while stage i is decoded (ring indices are compile-time
+        // because the stage loop is unrolled by the ring depth)
+        constexpr int D = 4;
+        uint32_t ring[D][KB], ringx[D];
+#pragma unroll
+        for (int d = 0; d < D - 1; ++d) {
+            if (d < nstages) {
+                tc_load_group<KB>(row_codes, ok, d, gi, ring[d], ringx[d]);
             } else {
 #pragma unroll
-                for (int q = 0; q < KB; ++q) nw[q] = 0u;
+                for (int q = 0; q < KB; ++q) ring[d][q] = 0u;
+                ringx[d] = 0u;
             }
-            uint32_t w[KB + 1];
+        }
+        bool alive = true;
+        for (int i0 = 0; i0 < nstages && alive; i0 += D) {
 #pragma unroll
-            for (int q = 0; q < KB; ++q) w[q] = cw[q];
-            const uint32_t nb = __shfl_sync(0xffffffffu, cw[0], src_lane);
-            w[KB] = (gi == 0) ? cx : nb;
+            for (int d = 0; d < D; ++d) {
+                const int i = i0 + d;
+                if (i >= nstages || !alive) break;
+                const int s = i % kTcStages;
+                const int pre = i + D - 1;
+                if (pre < nstages) {
+                    tc_load_group<KB>(row_codes, ok, pre, gi, ring[(d + D - 1) % D], ringx[(d + D - 1) % D]);
+                }
+                uint32_t w[KB + 1];
+#pragma unroll
+                for (int q = 0; q < KB; ++q) w[q] = ring[d][q];
+                const uint32_t nb = __shfl_sync(0xffffffffu, ring[d][0], src_lane);
+                w[KB] = (gi == 0) ? ringx[d] : nb;
 
-            uint32_t packed[16];
+                uint32_t packed[16];
 #pragma unroll
-            for (int jp = 0; jp < 16; ++jp) {
-                const float2 v = make_float2(tc_quotient(group_window<KB>(w, 2 * jp), lane_tbl),
-                                             tc_quotient(group_window<KB>(w, 2 * jp + 1), lane_tbl));
-                const float2 ws = __fmul2_rn(v, s2);
-                packed[jp] = pack_bf16x2(ws.x, ws.y);
+                for (int jp = 0; jp < 16; ++jp) {
+                    float2 v;
+                    if constexpr (kTcLut) {
+                        v = make_float2(tc_quotient(group_window<KB>(w, 2 * jp), lane_tbl),
+                                        tc_quotient(group_window<KB>(w, 2 * jp + 1), lane_tbl));
+                    } else {
+                        v = make_float2(window_value(group_window<KB>(w, 2 * jp)),
+                                        window_value(group_window<KB>(w, 2 * jp + 1)));
+                    }
+                    const float2 ws = __fmul2_rn(v, s2);
+                    packed[jp] = pack_bf16x2(ws.x, ws.y);
+                }
+                if (i >= kTcStages) alive = mbar_wait(bar_empty + 8 * s, ((i / kTcStages) + 1) & 1);
+                if (!alive) break;
+                const uint32_t dst = sbase + kOffA + s * kABytes + a_row_off;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 :: "r"(dst + q * kCoreLBO), "r"(packed[4 * q]), "r"(packed[4 * q + 1]),
+                                    "r"(packed[4 * q + 2]), "r"(packed[4 * q + 3]) : "memory");
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_full + 8 * s);
             }
-            if (i >= kTcStages) alive = mbar_wait(bar_empty + 8 * s, ((i >> 1) + 1) & 1);
-            if (!alive) break;
-            const uint32_t dst = sbase + kOffA + s * kABytes + a_row_off;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                             :: "r"(dst + q * kCoreLBO), "r"(packed[4 * q]), "r"(packed[4 * q + 1]),
-                                "r"(packed[4 * q + 2]), "r"(packed[4 * q + 3]) : "memory");
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_full + 8 * s);
-#pragma unroll
-            for (int q = 0; q < KB; ++q) cw[q] = nw[q];
-            cx = nx;
         }
 
         // -------------------------------------------------------------- epilogue
@@ -288,8 +314,8 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         // ------------------------------------------------------------- x via TMA
         if (lane == 0) {
             for (int i = 0; i < nstages; ++i) {
-                const int s = i & 1;
-                if (i >= kTcStages && !mbar_wait(bar_empty + 8 * s, ((i >> 1) + 1) & 1)) break;
+                const int s = i % kTcStages;
+                if (i >= kTcStages && !mbar_wait(bar_empty + 8 * s, ((i / kTcStages) + 1) & 1)) break;
                 mbar_arrive_expect_tx(bar_full + 8 * s, kBBytes);
                 const uint32_t dst = sbase + kOffB + s * kBBytes;
 #pragma unroll
@@ -302,8 +328,8 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         if (lane == 0) {
             bool ok = true;
             for (int i = 0; i < nstages; ++i) {
-                const int s = i & 1;
-                if (!mbar_wait(bar_full + 8 * s, (i >> 1) & 1)) { ok = false; break; }
+                const int s = i % kTcStages;
+                if (!mbar_wait(bar_full + 8 * s, (i / kTcStages) & 1)) { ok = false; break; }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t a0 = sbase + kOffA + s * kABytes;
                 const uint32_t b0 = sbase + kOffB + s * kBBytes;
