@@ -50,6 +50,23 @@ ALU_LANES_PER_SM = 128            # 4 sub-partitions x 32 lanes, one op per lane
 
 
 # ----------------------------------------------------------------- helpers --
+def max_over_ranks(vals, device="cpu"):
+    """Element-wise maximum of `vals` over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_gbs(world: int, bytes_per_rank: int, ms_per_step_max: float) -> float:
+    """Weak scaling: every rank processes its own copy of the workload, the job
+    takes as long as the slowest rank."""
+    return world * bytes_per_rank / (ms_per_step_max * 1e-3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -261,10 +278,7 @@ def run_ours(args, wl):
     total_ms = starts[0].elapsed_time(ends[-1])
     ms_step = total_ms / args.steps
     kernel_ms = statistics.mean(per_launch_ms)
-    if world > 1:
-        t = torch.tensor([ms_step, kernel_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, kernel_ms = float(t[0]), float(t[1])
+    ms_step, kernel_ms = max_over_ranks([ms_step, kernel_ms], device="cuda")
 
     # ---- end to end through the public API, host buffers in pinned memory ----
     e2e = None
@@ -308,12 +322,9 @@ def run_ours(args, wl):
             e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t[0])
+        (e2e_ms,) = max_over_ranks([e2e_ms], device="cuda")
         h2d = (hx.numel() * 2 if args.entry == "gemm" else 0) + hc.numel() * 4 + hs.numel() * 2
-        e2e = {"value": round(world * wl.code_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e2e = {"value": round(whole_job_gbs(world, wl.code_bytes, e2e_ms), 2), "unit": "GB/s",
                "us_per_call": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": hout.numel() * 2}
 
@@ -374,7 +385,7 @@ def run_ours(args, wl):
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} rows x K={wl.K} of {wl.name} (decode + product), {dt:.1f} s wall"}
 
-    value = world * wl.code_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(world, wl.code_bytes, ms_step)
     line = {
         "metric": METRIC if args.entry == "gemm" else METRIC_DECODE, "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world,
