@@ -18,10 +18,10 @@
 //    block) pairs, numbered tile-group-major, and CTA c takes the contiguous
 //    unit range [c*U/P, (c+1)*U/P): every SM gets the same number of weights
 //    whatever N and K are (stream-K split).  All warps of a CTA walk the same
-//    blocks in step, so the CTA stages x one block ahead, as fp32, through a
-//    two-slot shared-memory ring ([group][m][32 k], groups padded by 16 bytes
+//    blocks in step, so the CTA stages x UB blocks ahead, as fp32, through a
+//    2*UB-slot shared-memory ring ([group][m][32 k], groups padded by 16 bytes
 //    so the 8 groups of a load hit 8 different bank quads), with one CTA
-//    barrier per block.
+//    barrier per UB blocks.
 //  * At the end of a row segment the 8 lanes of a slot add their per-group
 //    sums by butterfly shuffles.  A row whose K-range is split over several
 //    CTAs writes fp32 partial sums to the workspace; the last CTA to finish a
@@ -60,7 +60,7 @@ struct SmallMPlan {
 //   WARPS  warps per CTA (= tiles per tile-group)
 //   LUT    decode the quotient through a shared-memory table instead of the
 //          three-op residual correction (same bits either way)
-template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1>
+template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1, int UB_ = 2>
 struct SmallMCfg {
     static constexpr int MM = MM_;
     static constexpr int R = R_;
@@ -74,7 +74,9 @@ struct SmallMCfg {
     static constexpr int NT = WARPS * 32;
     static constexpr int XV = MM * 32;                            // 8-element x vectors per block
     static constexpr int XPT = (XV + NT - 1) / NT;                // x vectors staged per thread per block
-    static constexpr size_t SMEM_BYTES = TABLE_BYTES + 2 * XS_UNIT * sizeof(float);
+    static constexpr int UB = UB_;                                // blocks per CTA barrier
+    static constexpr int RING = 2 * UB;                           // x ring slots
+    static constexpr size_t SMEM_BYTES = TABLE_BYTES + RING * XS_UNIT * sizeof(float);
 };
 
 // The shape used by the library for each M (chosen by timing the M = 1, 5, 8
@@ -96,16 +98,17 @@ __device__ __forceinline__ void load_block_group(const uint32_t* const (&rp)[R],
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         if (ok[r]) {
+            // volatile: issued where written (a block ahead of its use), never
+            // sunk toward the use to shorten register lifetimes
             const uint32_t* p = rp[r] + b * WPB + (kGroupsPerBlock - 1 - g) * KB;
             if constexpr (KB == 4) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-                w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
+                asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w[r][0]), "=r"(w[r][1]), "=r"(w[r][2]), "=r"(w[r][3]) : "l"(p));
             } else if constexpr (KB == 2) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-                w[r][0] = v.x; w[r][1] = v.y;
+                asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[r][0]), "=r"(w[r][1]) : "l"(p));
             } else {
 #pragma unroll
-                for (int i = 0; i < KB; ++i) w[r][i] = __ldg(p + i);
+                for (int i = 0; i < KB; ++i) asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[r][i]) : "l"(p + i));
             }
         } else {
 #pragma unroll
@@ -173,11 +176,15 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     if constexpr (C::LUT) build_quotient_table(reinterpret_cast<float*>(smem_raw), tid, NT);
     const uint32_t lane_tbl = quotient_table_lane_address(smem_raw, lane);
 
-    // Stage x of the first unit into ring slot 0.
-    if (u0 < u1) {
-        uint4 xv0[C::XPT];
-        x_block_load<C>(x, p.K, static_cast<int>(u0 % p.nblocks), tid, xv0);
-        x_block_store<C>(xs, tid, xv0);
+    constexpr int UB = C::UB, RING = C::RING;
+    // Stage x of the first UB units into ring slots 0 .. UB-1.
+#pragma unroll
+    for (int j = 0; j < UB; ++j) {
+        if (u0 + j < u1) {
+            uint4 xv0[C::XPT];
+            x_block_load<C>(x, p.K, static_cast<int>((u0 + j) % p.nblocks), tid, xv0);
+            x_block_store<C>(xs + j * XS_UNIT, tid, xv0);
+        }
     }
     __syncthreads();
 
@@ -189,18 +196,33 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     uint32_t cw[R][KB];
     int tg = -1, row0 = 0, tile = 0, b_first = 0;
     bool live = false;
+    // x of the next UB units: loaded at the start of a phase of UB units,
+    // stored to the ring (into the previous phase's slots) at its end, then
+    // one CTA barrier.
+    uint4 xnext[UB][C::XPT];
 
-    for (long long u = u0; u < u1; ++u) {
-        const int ring = static_cast<int>(u - u0) & 1;
-        const int utg = static_cast<int>(u / p.nblocks);
-        const int b = static_cast<int>(u - static_cast<long long>(utg) * p.nblocks);
-        const bool seg_start = (u == u0) || (b == 0);
-        const bool seg_end = (u + 1 == u1) || (b + 1 == p.nblocks);
+    // (tile-group, block) of the current unit, advanced incrementally: no
+    // 64-bit divisions inside the loop (unit indices fit in 32 bits: the host
+    // limits N*K/256 to below 2^31)
+    const int nunits = static_cast<int>(u1 - u0);
+    int utg = first_tg;
+    int b = static_cast<int>(u0 - static_cast<long long>(first_tg) * p.nblocks);
+    for (int rel = 0; rel < nunits; ++rel) {
+        const int ring = rel % RING;
+        const bool seg_start = (rel == 0) || (b == 0);
+        const bool seg_end = (rel + 1 == nunits) || (b + 1 == p.nblocks);
+        const bool phase_start = (rel % UB) == 0;
+        const bool phase_end = (rel % UB) == UB - 1 || rel + 1 == nunits;
 
-        // x of the next unit: loads now, shared stores after this unit's work
-        uint4 xnext[C::XPT];
-        const bool have_next = u + 1 < u1;
-        if (have_next) x_block_load<C>(x, p.K, static_cast<int>((u + 1) % p.nblocks), tid, xnext);
+        if (phase_start) {
+#pragma unroll
+            for (int j = 0; j < UB; ++j)
+                if (rel + UB + j < nunits) {
+                    int bj = b + UB + j;
+                    while (bj >= p.nblocks) bj -= p.nblocks;
+                    x_block_load<C>(x, p.K, bj, tid, xnext[j]);
+                }
+        }
 
         if (seg_start) {
             tg = utg;
@@ -224,7 +246,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         if (live) {
             // the block after next: pull it toward L2 now, so the register
             // prefetch issued one unit ahead finds it there
-            if (b + 2 < p.nblocks && u + 2 < u1) {
+            if (b + 2 < p.nblocks && rel + 2 < nunits) {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
                     if (ok[r] && g == 0)
@@ -365,8 +387,19 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             }
         }
 
-        if (have_next) x_block_store<C>(xs + (ring ^ 1) * XS_UNIT, tid, xnext);
-        __syncthreads();
+        if (phase_end) {
+            const int pbase = rel - (rel % UB);
+#pragma unroll
+            for (int j = 0; j < UB; ++j) {
+                const int rn = pbase + UB + j;
+                if (rn < nunits) x_block_store<C>(xs + (rn % RING) * XS_UNIT, tid, xnext[j]);
+            }
+            __syncthreads();
+        }
+        if (++b == p.nblocks) {
+            b = 0;
+            ++utg;
+        }
     }
 }
 
