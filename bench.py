@@ -254,8 +254,11 @@ def run_ours(args, wl):
             call(i)
     torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # The K steps run back to back on one stream (as a model issues its
+    # layers), bracketed by one pair of events; each step is one launch, so
+    # the average launch duration is the step time.
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.15)
@@ -264,21 +267,31 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     t_host0 = time.perf_counter()
     with torch.cuda.stream(stream):
+        t_start.record(stream)
         for i in range(args.steps):
-            starts[i].record(stream)
             call(args.warmup + i)
-            ends[i].record(stream)
+        t_end.record(stream)
     torch.cuda.synchronize()
     t_host = time.perf_counter() - t_host0
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = starts[0].elapsed_time(ends[-1])
+    total_ms = t_start.elapsed_time(t_end)
     ms_step = total_ms / args.steps
-    kernel_ms = statistics.mean(per_launch_ms)
-    ms_step, kernel_ms = max_over_ranks([ms_step, kernel_ms], device="cuda")
+    kernel_ms = ms_step
+
+    # For context, outside the timed region: one call at a time, each between
+    # its own pair of events (adds the launch and drain latency to every call).
+    n_iso = min(args.steps, 50)
+    iso = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_iso)]
+    with torch.cuda.stream(stream):
+        for i, (a, b) in enumerate(iso):
+            a.record(stream)
+            call(args.warmup + args.steps + i)
+            b.record(stream)
+    torch.cuda.synchronize()
+    isolated_ms = statistics.median([a.elapsed_time(b) for a, b in iso])
+    ms_step, kernel_ms, isolated_ms = max_over_ranks([ms_step, kernel_ms, isolated_ms], device="cuda")
 
     # ---- end to end through the public API, host buffers in pinned memory ----
     e2e = None
@@ -390,7 +403,8 @@ def run_ours(args, wl):
         "metric": METRIC if args.entry == "gemm" else METRIC_DECODE, "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "us_per_call": round(ms_step * 1e3, 2), "isolated_call_us": round(isolated_ms * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "entry": "trellis_" + args.entry, "M": wl.M, "K": wl.K, "N": wl.N,
                    "k": wl.k, "L": wl.L, "T": wl.T, "parallelism": f"replicas{world}",

@@ -177,6 +177,35 @@ def test_gemm_workspace_reuse_across_geometries(tq, oracle_lib):
         assert int(ws[: 1 << 20].count_nonzero()) == 0, "tile counters not left at zero"
 
 
+def test_gemm_back_to_back_chain(tq, oracle_lib):
+    """Calls queued back to back on one stream with no synchronisation between
+    them: each layer's output is the next layer's activations, and all share one
+    workspace.  A launch may begin while the previous one drains, so this checks
+    that every input a call reads, and the workspace, are complete before use."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    M = 8
+    layers = [(512, 768, 3), (768, 1280, 4), (1280, 256, 2), (256, 5120, 3), (5120, 512, 4)]
+    weights = [_inputs(M, K, N, k, seed=1300 + i)[1:] for i, (K, N, k) in enumerate(layers)]
+    x0 = _inputs(M, layers[0][0], 1, 2, seed=1299)[0]
+    need = max(binding.gemm_workspace_bytes(M, K, N, k) for K, N, k in layers)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    acts = [dev_bf16(x0)] + [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _, N, _ in layers]
+    dev_w = [(dev_codes(c), dev_bf16(sc)) for c, sc in weights]
+    torch.cuda.synchronize()
+    for i, ((K, N, k), (dc, ds)) in enumerate(zip(layers, dev_w)):
+        assert binding.abi_gemm_ws(acts[i].data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256,
+                                   acts[i + 1].data_ptr(), ws.data_ptr(), need, s) == 0
+    torch.cuda.synchronize()
+    for i, ((K, N, k), (codes, scales)) in enumerate(zip(layers, weights)):
+        x = host_bits(acts[i])           # the GPU's own input to this layer
+        w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+        ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+        assert_gemm_close(host_bits(acts[i + 1]), ref, refabs, f"layer {i}")
+    assert int(ws[: 1 << 20].count_nonzero()) == 0, "tile counters not left at zero"
+
+
 def test_gemm_workspace_errors(tq):
     import torch
     from trellis_quantized_weight_gb300 import binding

@@ -24,10 +24,13 @@
 //    barrier per UB blocks.
 //  * At the end of a row segment the 8 lanes of a slot add their per-group
 //    sums by butterfly shuffles.  A row whose K-range is split over several
-//    CTAs writes fp32 partial sums to the workspace; the last CTA to finish a
-//    tile (ticket from a per-tile counter) adds the partials in CTA order,
-//    rounds to bf16, stores and resets the counter.  The sum order is fixed:
-//    identical inputs give identical bits.  No CTA ever waits on another.
+//    CTAs writes fp32 partial sums to the workspace as soon as its segment
+//    ends; only a CTA's first and last segments can be split, and both take
+//    their per-tile tickets after the CTA's last unit, so the loop never waits
+//    on a fence or an atomic.  The last CTA to take a tile's ticket adds the
+//    partials in CTA order, rounds to bf16, stores and resets the counter.
+//    The sum order is fixed: identical inputs give identical bits.  No CTA
+//    ever waits on another.
 //  * Decode per weight: funnel shift + mask, hash IMAD, then either the dp4a
 //    byte sum into a float and the 3-op residual-corrected quotient, or one
 //    dp4a that turns the hash into the address of the quotient in a per-lane
@@ -49,8 +52,8 @@ struct SmallMPlan {
     int row_words;      // K * k / 32
     int ntg;            // tile-groups
     int P;              // CTAs
-    int units_max;      // ceil(U / P)
-    long long U;        // units = ntg * nblocks
+    int U;              // units = ntg * nblocks (below 2^31: N*K/256 is)
+    int base, rem;      // CTA c takes base + (c < rem) units, c*base + min(c, rem) first
     float* partials;    // workspace: [P][2][WARPS][R*M*4] fp32
     uint32_t* counters; // workspace: [ntg * WARPS]
 };
@@ -86,10 +89,19 @@ struct SmallMDefault {
     using type = SmallMCfg<MM, (MM <= 5) ? 4 : 3, (MM <= 7) ? 16 : (MM <= 11 ? 12 : 8), true>;
 };
 
-__device__ __forceinline__ int cta_of_unit(long long u, long long U, int P) {
-    const long long c = ((u + 1) * P - 1) / U;
-    return static_cast<int>(c < P - 1 ? c : P - 1);
+__device__ __forceinline__ int unit_begin(int c, const SmallMPlan& p) {
+    return c * p.base + (c < p.rem ? c : p.rem);
 }
+
+__device__ __forceinline__ int cta_of_unit(int u, const SmallMPlan& p) {
+    const int big = p.rem * (p.base + 1);   // units of the CTAs that take base + 1
+    return u < big ? u / (p.base + 1) : p.rem + (u - big) / p.base;
+}
+
+// Release/acquire fence at GPU scope: orders this thread's partial-sum
+// stores before its ticket, and the last contributor's ticket before its
+// loads of the other CTAs' partial sums.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 template <int KB, int R>
 __device__ __forceinline__ void load_block_group(const uint32_t* const (&rp)[R], const bool (&ok)[R], int b,
@@ -155,38 +167,83 @@ __device__ __forceinline__ void x_block_store(float* slot, int tid, const uint4 
     }
 }
 
+// Sum of the partial sums of one split tile in CTA order, by its last
+// contributor; every load is issued before the first add.
+template <class C>
+__device__ __forceinline__ void reduce_split_tile(const SmallMPlan& p, int tg, int warp, int lane,
+                                                  uint16_t* __restrict__ out) {
+    constexpr int MM = C::MM, WARPS = C::WARPS;
+    constexpr int E = C::R * MM * 4;                  // sums of one warp's tile
+    constexpr int EP = (E + 31) / 32;                 // sums per lane
+    const int tg_u0 = tg * p.nblocks;
+    const int c_first = cta_of_unit(tg_u0, p);
+    const int c_last = cta_of_unit(tg_u0 + p.nblocks - 1, p);
+    // Every CTA after c_first starts inside this tile-group, so this
+    // tile-group is its first (slot 0); c_first used slot 1 unless its range
+    // also starts at the tile-group's first unit.
+    const int cf_slot = (unit_begin(c_first, p) < tg_u0) ? 1 : 0;
+    const int tile = tg * WARPS + warp;
+    const int row0 = tile * C::ROWS_PER_TILE;
+
+    float sum[EP];
+#pragma unroll
+    for (int ep = 0; ep < EP; ++ep) sum[ep] = 0.0f;
+    for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
+        float part[EP][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int cc = cc0 + i;
+            const int cs = (cc == c_first) ? cf_slot : 0;
+            const float* src = p.partials + ((static_cast<size_t>(cc) * 2 + cs) * WARPS + warp) * E;
+#pragma unroll
+            for (int ep = 0; ep < EP; ++ep) {
+                const int e = lane + 32 * ep;
+                part[ep][i] = (cc <= c_last && e < E) ? __ldcg(src + e) : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (cc0 + i <= c_last)
+#pragma unroll
+                for (int ep = 0; ep < EP; ++ep) sum[ep] = __fadd_rn(sum[ep], part[ep][i]);
+    }
+#pragma unroll
+    for (int ep = 0; ep < EP; ++ep) {
+        const int e = lane + 32 * ep;
+        if (e < E) {
+            const int q = e & 3, rm = e >> 2;
+            const int r = rm / MM, m = rm - r * MM;
+            const int n = row0 + q + 4 * r;
+            if (n < p.N) out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum[ep]);
+        }
+    }
+    if (lane == 0) p.counters[tile] = 0u;
+}
+
 template <class C, int KB>
 __global__ void __launch_bounds__(C::WARPS * 32, C::OCC)
 gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes,
                    const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, SmallMPlan p) {
     constexpr int MM = C::MM, R = C::R, WARPS = C::WARPS, XG = C::XG, XS_UNIT = C::XS_UNIT;
     constexpr int NT = C::NT;
+    constexpr int UB = C::UB, RING = C::RING;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float* xs = reinterpret_cast<float*>(smem_raw + C::TABLE_BYTES);   // 2 ring slots of XS_UNIT floats
+    float* xs = reinterpret_cast<float*>(smem_raw + C::TABLE_BYTES);   // RING slots of XS_UNIT floats
 
     const int c = blockIdx.x;
-    const long long u0 = static_cast<long long>(c) * p.U / p.P;
-    const long long u1 = static_cast<long long>(c + 1) * p.U / p.P;
+    const int u0 = unit_begin(c, p);
+    const int u1 = unit_begin(c + 1, p);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane & 7, slot = lane >> 3;
     const int src_lane = (g == 0) ? lane + 7 : lane - 1;
-    const int first_tg = static_cast<int>(u0 / p.nblocks);
+    const int first_tg = u0 / p.nblocks;
 
-    if constexpr (C::LUT) build_quotient_table(reinterpret_cast<float*>(smem_raw), tid, NT);
-    const uint32_t lane_tbl = quotient_table_lane_address(smem_raw, lane);
-
-    constexpr int UB = C::UB, RING = C::RING;
-    // Stage x of the first UB units into ring slots 0 .. UB-1.
-#pragma unroll
-    for (int j = 0; j < UB; ++j) {
-        if (u0 + j < u1) {
-            uint4 xv0[C::XPT];
-            x_block_load<C>(x, p.K, static_cast<int>((u0 + j) % p.nblocks), tid, xv0);
-            x_block_store<C>(xs + j * XS_UNIT, tid, xv0);
-        }
-    }
-    __syncthreads();
+    // (tile-group, block) of the current unit, advanced incrementally: no
+    // divisions inside the loop
+    const int nunits = u1 - u0;
+    int utg = first_tg;
+    int b = u0 - first_tg * p.nblocks;
 
     // Per-segment state of this warp's tile.
     bool ok[R];
@@ -196,17 +253,58 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     uint32_t cw[R][KB];
     int tg = -1, row0 = 0, tile = 0, b_first = 0;
     bool live = false;
+    auto begin_segment = [&]() {
+        tg = utg;
+        b_first = b;
+        tile = tg * WARPS + warp;
+        row0 = tile * C::ROWS_PER_TILE;
+        live = row0 < p.N;   // whole tile beyond N: skipped by every CTA alike
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int n = row0 + slot + 4 * r;
+            ok[r] = n < p.N;
+            const float sr = ok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
+            s2[r] = make_float2(sr, sr);
+            rp[r] = codes + static_cast<size_t>(ok[r] ? n : 0) * p.row_words;
+#pragma unroll
+            for (int m = 0; m < MM; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
+        }
+        if (live) load_block_group<KB, R>(rp, ok, b, g, cw);
+    };
+
+    // Shared-memory set-up first: under a programmatic launch it overlaps the
+    // previous kernel's tail.  No global memory is read or written before
+    // griddep_wait().  Then the first segment's codes and the x of the first
+    // UB units (into ring slots 0 .. UB-1).
+    if constexpr (C::LUT) build_quotient_table(reinterpret_cast<float*>(smem_raw), tid, NT);
+    griddep_wait();
+    if (nunits > 0) begin_segment();
+    {
+        uint4 xfirst[UB][C::XPT];
+#pragma unroll
+        for (int j = 0; j < UB; ++j)
+            if (j < nunits) {
+                int bj = b + j;
+                while (bj >= p.nblocks) bj -= p.nblocks;
+                x_block_load<C>(x, p.K, bj, tid, xfirst[j]);
+            }
+#pragma unroll
+        for (int j = 0; j < UB; ++j)
+            if (j < nunits) x_block_store<C>(xs + j * XS_UNIT, tid, xfirst[j]);
+    }
+    __syncthreads();
+    const uint32_t lane_tbl = quotient_table_lane_address(smem_raw, lane);
+
     // x of the next UB units: loaded at the start of a phase of UB units,
     // stored to the ring (into the previous phase's slots) at its end, then
     // one CTA barrier.
     uint4 xnext[UB][C::XPT];
+    // Split segments (at most two per CTA: its first and its last) publish
+    // their partial sums at once; their tickets are taken after the loop, so
+    // no fence or atomic round trip stalls the loop.  Indexed by partial slot.
+    bool pend0 = false, pend1 = false;
+    int ptg0 = 0, ptg1 = 0;
 
-    // (tile-group, block) of the current unit, advanced incrementally: no
-    // 64-bit divisions inside the loop (unit indices fit in 32 bits: the host
-    // limits N*K/256 to below 2^31)
-    const int nunits = static_cast<int>(u1 - u0);
-    int utg = first_tg;
-    int b = static_cast<int>(u0 - static_cast<long long>(first_tg) * p.nblocks);
     for (int rel = 0; rel < nunits; ++rel) {
         const int ring = rel % RING;
         const bool seg_start = (rel == 0) || (b == 0);
@@ -224,24 +322,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 }
         }
 
-        if (seg_start) {
-            tg = utg;
-            b_first = b;
-            tile = tg * WARPS + warp;
-            row0 = tile * C::ROWS_PER_TILE;
-            live = row0 < p.N;   // whole tile beyond N: skipped by every CTA alike
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int n = row0 + slot + 4 * r;
-                ok[r] = n < p.N;
-                const float sr = ok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
-                s2[r] = make_float2(sr, sr);
-                rp[r] = codes + static_cast<size_t>(ok[r] ? n : 0) * p.row_words;
-#pragma unroll
-                for (int m = 0; m < MM; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
-            }
-            if (live) load_block_group<KB, R>(rp, ok, b, g, cw);
-        }
+        if (seg_start && rel > 0) begin_segment();
 
         if (live) {
             // the block after next: pull it toward L2 now, so the register
@@ -331,7 +412,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                             if ((m & 7) == g)
                                 out[static_cast<size_t>(m) * p.N + row0 + slot + 4 * r] = bf16_bits_rn(v[r][m]);
             } else {
-                // ---- split row: publish the partial, the last arriver reduces ----
+                // ---- split row: publish the partial now, take the ticket after the loop ----
                 // element (r, m) of row slot q sits at [(r*MM + m)*4 + q]; lane g == 0 writes
                 const int pslot = (tg == first_tg) ? 0 : 1;
                 float* mine = p.partials + ((static_cast<size_t>(c) * 2 + pslot) * WARPS + warp) * (R * MM * 4);
@@ -341,48 +422,12 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 #pragma unroll
                         for (int m = 0; m < MM; ++m) mine[(r * MM + m) * 4 + slot] = v[r][m];
                 }
-                __threadfence();
-                __syncwarp();
-                uint32_t ticket = 0;
-                if (lane == 0) ticket = atomicAdd(p.counters + tile, 1u);
-                ticket = __shfl_sync(0xffffffffu, ticket, 0);
-                const long long tg_u0 = static_cast<long long>(tg) * p.nblocks;
-                const int c_first = cta_of_unit(tg_u0, p.U, p.P);
-                const int c_last = cta_of_unit(tg_u0 + p.nblocks - 1, p.U, p.P);
-                if (ticket == static_cast<uint32_t>(c_last - c_first)) {
-                    __threadfence();
-                    // Every CTA after c_first starts inside this tile-group, so
-                    // this tile-group is its first (slot 0); c_first used slot 1
-                    // unless its range also starts at the tile-group's first unit.
-                    const long long cf_u0 = static_cast<long long>(c_first) * p.U / p.P;
-                    const int cf_slot = (cf_u0 < tg_u0) ? 1 : 0;
-                    constexpr int E = R * MM * 4;
-                    // the 32 lanes share the E sums of the tile; partials are
-                    // loaded 8 CTAs at a time and added in CTA order
-                    for (int e = lane; e < E; e += 32) {
-                        float sum = 0.0f;
-                        for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
-                            float part[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int cc = cc0 + i;
-                                part[i] = 0.0f;
-                                if (cc <= c_last) {
-                                    const int cs = (cc == c_first) ? cf_slot : 0;
-                                    part[i] = __ldcg(p.partials +
-                                                     ((static_cast<size_t>(cc) * 2 + cs) * WARPS + warp) * E + e);
-                                }
-                            }
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                if (cc0 + i <= c_last) sum = __fadd_rn(sum, part[i]);
-                        }
-                        const int q = e & 3, rm = e >> 2;
-                        const int r = rm / MM, m = rm - r * MM;
-                        const int n = row0 + q + 4 * r;
-                        if (n < p.N) out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum);
-                    }
-                    if (lane == 0) p.counters[tile] = 0u;
+                if (pslot == 0) {
+                    pend0 = true;
+                    ptg0 = tg;
+                } else {
+                    pend1 = true;
+                    ptg1 = tg;
                 }
             }
         }
@@ -399,6 +444,33 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         if (++b == p.nblocks) {
             b = 0;
             ++utg;
+        }
+    }
+
+    // the next grid on the stream may be scheduled as this CTA's SM frees up
+    griddep_launch_dependents();
+
+    // ---- tickets of the split segments; the last contributor of a tile reduces it ----
+    if (pend0 || pend1) {
+        fence_acq_rel_gpu();   // this warp's partial sums are visible before its tickets
+        __syncwarp();
+        uint32_t t0 = 0, t1 = 0;
+        if (lane == 0) {
+            if (pend0) t0 = atomicAdd(p.counters + ptg0 * WARPS + warp, 1u);
+            if (pend1) t1 = atomicAdd(p.counters + ptg1 * WARPS + warp, 1u);
+        }
+        t0 = __shfl_sync(0xffffffffu, t0, 0);
+        t1 = __shfl_sync(0xffffffffu, t1, 0);
+        auto contributors = [&](int t) {
+            const int tg_u0 = t * p.nblocks;
+            return cta_of_unit(tg_u0 + p.nblocks - 1, p) - cta_of_unit(tg_u0, p) + 1;
+        };
+        const bool last0 = pend0 && t0 == static_cast<uint32_t>(contributors(ptg0) - 1);
+        const bool last1 = pend1 && t1 == static_cast<uint32_t>(contributors(ptg1) - 1);
+        if (last0 || last1) {
+            fence_acq_rel_gpu();
+            if (last0) reduce_split_tile<C>(p, ptg0, warp, lane, out);
+            if (last1) reduce_split_tile<C>(p, ptg1, warp, lane, out);
         }
     }
 }
@@ -421,11 +493,12 @@ SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev) {
     p.row_words = K / 32 * k;
     const int rows_per_tg = C::WARPS * C::ROWS_PER_TILE;
     p.ntg = (N + rows_per_tg - 1) / rows_per_tg;
-    p.U = static_cast<long long>(p.ntg) * p.nblocks;
-    long long P = static_cast<long long>(dev.num_sms) * C::OCC;
+    p.U = p.ntg * p.nblocks;
+    int P = dev.num_sms * C::OCC;
     if (P > p.U) P = p.U;
-    p.P = static_cast<int>(P);
-    p.units_max = static_cast<int>((p.U + P - 1) / P);
+    p.P = P;
+    p.base = p.U / P;
+    p.rem = p.U % P;
     return p;
 }
 
@@ -458,8 +531,10 @@ int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint1
             return -5;
         attr_set = true;
     }
-    gemm_smallm_kernel<C, KB><<<p.P, C::WARPS * 32, smem, stream>>>(x, codes, scales, out, p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+    const cudaError_t e = launch_programmatic(gemm_smallm_kernel<C, KB>, static_cast<unsigned>(p.P),
+                                              static_cast<unsigned>(C::WARPS * 32), smem, stream,
+                                              x, codes, scales, out, p);
+    return e == cudaSuccess ? 0 : -5;
 }
 
 template <int KB>

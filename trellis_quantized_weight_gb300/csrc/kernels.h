@@ -19,6 +19,27 @@ struct DeviceInfo {
     int max_smem_optin = 0;   // bytes of dynamic shared memory a CTA may opt into
 };
 
+// Launch with programmatic stream serialization: the grid may begin while the
+// previous kernel on the stream is still draining.  Kernels launched this way
+// touch no global memory before griddepcontrol.wait, which returns once the
+// previous grid has completed and its writes are visible, so stream order is
+// kept for every input and output.
+template <class... Params, class... Args>
+cudaError_t launch_programmatic(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                                cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Dense decode of all N rows into out [N, K].  Returns 0 or a trellis_status.
 int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
                   uint16_t* out, cudaStream_t stream, const DeviceInfo& dev);

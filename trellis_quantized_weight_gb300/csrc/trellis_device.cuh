@@ -66,6 +66,15 @@ __device__ __forceinline__ float window_value(uint32_t win) {
     return code_to_value(__fsub_rn(biased, kMagicPlusBias));
 }
 
+// ---- programmatic dependent launch --------------------------------------------
+// Wait until the grids this launch depends on have completed and their writes
+// are visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next programmatically launched grid on the stream be scheduled.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- quotient table ---------------------------------------------------------
 // The value depends on the window only through the byte sum S = code + 510,
 // S in [0, 1020].  A shared-memory table holds value(S) once per lane:
