@@ -61,6 +61,7 @@ decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ s
         }
     };
 
+    griddep_wait();   // no global memory is touched before the previous grid's writes are visible
     uint32_t cw[KB];
     float cs = 0.0f;
     uint32_t base = warp * 4u;
@@ -118,6 +119,7 @@ decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ s
         for (int i = 0; i < KB; ++i) cw[i] = nw[i];
         cs = ns;
     }
+    griddep_launch_dependents();
     // the shared buffers must outlive the bulk copies that read them
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -132,13 +134,14 @@ int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, i
     const uint32_t max_ctas = static_cast<uint32_t>(dev.num_sms) * 6u;
     const uint32_t grid = ctas_needed < max_ctas ? ctas_needed : max_ctas;
     const FastDiv fd(blocks_per_row);
+    cudaError_t e;
     switch (k) {
-        case 2: decode_kernel<2><<<grid, kDecodeWarps * 32, 0, stream>>>(codes, scales, items, fd, out); break;
-        case 3: decode_kernel<3><<<grid, kDecodeWarps * 32, 0, stream>>>(codes, scales, items, fd, out); break;
-        case 4: decode_kernel<4><<<grid, kDecodeWarps * 32, 0, stream>>>(codes, scales, items, fd, out); break;
+        case 2: e = launch_programmatic(decode_kernel<2>, grid, kDecodeWarps * 32, 0, stream, codes, scales, items, fd, out); break;
+        case 3: e = launch_programmatic(decode_kernel<3>, grid, kDecodeWarps * 32, 0, stream, codes, scales, items, fd, out); break;
+        case 4: e = launch_programmatic(decode_kernel<4>, grid, kDecodeWarps * 32, 0, stream, codes, scales, items, fd, out); break;
         default: return -3;
     }
-    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+    return e == cudaSuccess ? 0 : -5;
 }
 
 }  // namespace trellis

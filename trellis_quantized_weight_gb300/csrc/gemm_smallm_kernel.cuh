@@ -98,10 +98,15 @@ __device__ __forceinline__ int cta_of_unit(int u, const SmallMPlan& p) {
     return u < big ? u / (p.base + 1) : p.rem + (u - big) / p.base;
 }
 
-// Release/acquire fence at GPU scope: orders this thread's partial-sum
-// stores before its ticket, and the last contributor's ticket before its
-// loads of the other CTAs' partial sums.
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// A tile's ticket: add 1 to its counter at GPU scope with release semantics
+// (the warp's partial-sum stores, ordered before it by a warp barrier, become
+// visible first) and acquire semantics (the last contributor's later loads of
+// the other CTAs' partial sums see them).  Returns the previous count.
+__device__ __forceinline__ uint32_t take_ticket(uint32_t* counter) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    return old;
+}
 
 template <int KB, int R>
 __device__ __forceinline__ void load_block_group(const uint32_t* const (&rp)[R], const bool (&ok)[R], int b,
@@ -167,57 +172,75 @@ __device__ __forceinline__ void x_block_store(float* slot, int tid, const uint4 
     }
 }
 
-// Sum of the partial sums of one split tile in CTA order, by its last
-// contributor; every load is issued before the first add.
+// Adds the partial sums of up to two split tiles of this warp (tile-groups
+// tgs[t] where use[t]) in CTA order, rounds to bf16, stores, and resets the
+// tiles' counters.  All loads of a round, for both tiles, are issued before
+// the first add, so the reduction costs one round trip per 8 contributors.
 template <class C>
-__device__ __forceinline__ void reduce_split_tile(const SmallMPlan& p, int tg, int warp, int lane,
-                                                  uint16_t* __restrict__ out) {
+__device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bool (&use)[2], const int (&tgs)[2],
+                                                   int warp, int lane, uint16_t* __restrict__ out) {
     constexpr int MM = C::MM, WARPS = C::WARPS;
     constexpr int E = C::R * MM * 4;                  // sums of one warp's tile
     constexpr int EP = (E + 31) / 32;                 // sums per lane
-    const int tg_u0 = tg * p.nblocks;
-    const int c_first = cta_of_unit(tg_u0, p);
-    const int c_last = cta_of_unit(tg_u0 + p.nblocks - 1, p);
-    // Every CTA after c_first starts inside this tile-group, so this
-    // tile-group is its first (slot 0); c_first used slot 1 unless its range
-    // also starts at the tile-group's first unit.
-    const int cf_slot = (unit_begin(c_first, p) < tg_u0) ? 1 : 0;
-    const int tile = tg * WARPS + warp;
-    const int row0 = tile * C::ROWS_PER_TILE;
-
-    float sum[EP];
+    int c_first[2], c_last[2], cf_slot[2];
+    int rounds = 0;
 #pragma unroll
-    for (int ep = 0; ep < EP; ++ep) sum[ep] = 0.0f;
-    for (int cc0 = c_first; cc0 <= c_last; cc0 += 8) {
-        float part[EP][8];
+    for (int t = 0; t < 2; ++t) {
+        const int tg_u0 = tgs[t] * p.nblocks;
+        c_first[t] = use[t] ? cta_of_unit(tg_u0, p) : 1;
+        c_last[t] = use[t] ? cta_of_unit(tg_u0 + p.nblocks - 1, p) : 0;
+        // Every CTA after c_first starts inside the tile-group, so the
+        // tile-group is its first (slot 0); c_first used slot 1 unless its
+        // range also starts at the tile-group's first unit.
+        cf_slot[t] = (use[t] && unit_begin(c_first[t], p) < tg_u0) ? 1 : 0;
+        const int r = (c_last[t] - c_first[t] + 8) >> 3;
+        rounds = r > rounds ? r : rounds;
+    }
+    float sum[2][EP];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int cc = cc0 + i;
-            const int cs = (cc == c_first) ? cf_slot : 0;
-            const float* src = p.partials + ((static_cast<size_t>(cc) * 2 + cs) * WARPS + warp) * E;
+    for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int ep = 0; ep < EP; ++ep) {
-                const int e = lane + 32 * ep;
-                part[ep][i] = (cc <= c_last && e < E) ? __ldcg(src + e) : 0.0f;
+        for (int ep = 0; ep < EP; ++ep) sum[t][ep] = 0.0f;
+    for (int rd = 0; rd < rounds; ++rd) {
+        float part[2][EP][8];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int cc = c_first[t] + 8 * rd + i;
+                const int cs = (cc == c_first[t]) ? cf_slot[t] : 0;
+                const float* src = p.partials + ((static_cast<size_t>(cc) * 2 + cs) * WARPS + warp) * E;
+#pragma unroll
+                for (int ep = 0; ep < EP; ++ep) {
+                    const int e = lane + 32 * ep;
+                    part[t][ep][i] = (cc <= c_last[t] && e < E) ? __ldcg(src + e) : 0.0f;
+                }
+            }
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (c_first[t] + 8 * rd + i <= c_last[t])
+#pragma unroll
+                    for (int ep = 0; ep < EP; ++ep) sum[t][ep] = __fadd_rn(sum[t][ep], part[t][ep][i]);
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (!use[t]) continue;
+        const int tile = tgs[t] * WARPS + warp;
+        const int row0 = tile * C::ROWS_PER_TILE;
+#pragma unroll
+        for (int ep = 0; ep < EP; ++ep) {
+            const int e = lane + 32 * ep;
+            if (e < E) {
+                const int q = e & 3, rm = e >> 2;
+                const int r = rm / MM, m = rm - r * MM;
+                const int n = row0 + q + 4 * r;
+                if (n < p.N) out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum[t][ep]);
             }
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (cc0 + i <= c_last)
-#pragma unroll
-                for (int ep = 0; ep < EP; ++ep) sum[ep] = __fadd_rn(sum[ep], part[ep][i]);
+        if (lane == 0) p.counters[tile] = 0u;
     }
-#pragma unroll
-    for (int ep = 0; ep < EP; ++ep) {
-        const int e = lane + 32 * ep;
-        if (e < E) {
-            const int q = e & 3, rm = e >> 2;
-            const int r = rm / MM, m = rm - r * MM;
-            const int n = row0 + q + 4 * r;
-            if (n < p.N) out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum[ep]);
-        }
-    }
-    if (lane == 0) p.counters[tile] = 0u;
 }
 
 template <class C, int KB>
@@ -452,26 +475,23 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 
     // ---- tickets of the split segments; the last contributor of a tile reduces it ----
     if (pend0 || pend1) {
-        fence_acq_rel_gpu();   // this warp's partial sums are visible before its tickets
-        __syncwarp();
+        __syncwarp();   // the slot lanes' partial-sum stores are ordered before lane 0's tickets
         uint32_t t0 = 0, t1 = 0;
         if (lane == 0) {
-            if (pend0) t0 = atomicAdd(p.counters + ptg0 * WARPS + warp, 1u);
-            if (pend1) t1 = atomicAdd(p.counters + ptg1 * WARPS + warp, 1u);
+            if (pend0) t0 = take_ticket(p.counters + ptg0 * WARPS + warp);
+            if (pend1) t1 = take_ticket(p.counters + ptg1 * WARPS + warp);
         }
         t0 = __shfl_sync(0xffffffffu, t0, 0);
         t1 = __shfl_sync(0xffffffffu, t1, 0);
+        __syncwarp();   // every lane's loads below are ordered after lane 0's acquire
         auto contributors = [&](int t) {
             const int tg_u0 = t * p.nblocks;
             return cta_of_unit(tg_u0 + p.nblocks - 1, p) - cta_of_unit(tg_u0, p) + 1;
         };
-        const bool last0 = pend0 && t0 == static_cast<uint32_t>(contributors(ptg0) - 1);
-        const bool last1 = pend1 && t1 == static_cast<uint32_t>(contributors(ptg1) - 1);
-        if (last0 || last1) {
-            fence_acq_rel_gpu();
-            if (last0) reduce_split_tile<C>(p, ptg0, warp, lane, out);
-            if (last1) reduce_split_tile<C>(p, ptg1, warp, lane, out);
-        }
+        const bool use[2] = {pend0 && t0 == static_cast<uint32_t>(contributors(ptg0) - 1),
+                             pend1 && t1 == static_cast<uint32_t>(contributors(ptg1) - 1)};
+        const int tgs[2] = {ptg0, ptg1};
+        if (use[0] || use[1]) reduce_split_tiles<C>(p, use, tgs, warp, lane, out);
     }
 }
 

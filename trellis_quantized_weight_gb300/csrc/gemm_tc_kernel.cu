@@ -213,6 +213,8 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t taddr = *reinterpret_cast<volatile uint32_t*>(smem + kOffTaddr);
+    // everything above is on-chip set-up; global memory only after this
+    griddep_wait();
 
     if (warp < kTcDecodeWarps) {
         // ---------------------------------------------------------------- decode
@@ -344,6 +346,7 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         }
     }
 
+    griddep_launch_dependents();
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == kTcMmaWarp) {
@@ -399,8 +402,10 @@ int launch_tc_instance(const uint16_t* x, const uint32_t* codes, const uint16_t*
         attr_set = true;
     }
     const int grid = (N + kTcRows - 1) / kTcRows;
-    gemm_tc_kernel<KB><<<grid, kTcThreads, kTcSmemBytes, stream>>>(codes, scales, out, K, N, K / 32 * KB, map);
-    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+    const cudaError_t e = launch_programmatic(gemm_tc_kernel<KB>, static_cast<unsigned>(grid),
+                                              static_cast<unsigned>(kTcThreads), kTcSmemBytes, stream,
+                                              codes, scales, out, K, N, K / 32 * KB, map);
+    return e == cudaSuccess ? 0 : -5;
 }
 
 }  // namespace
