@@ -25,11 +25,12 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
-import hashlib
 import glob
+import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -83,12 +84,21 @@ def measured_peaks():
             "sm_max_mhz": 2070.0}, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments, blank lines or indentation."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.strip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources' code (comments ignored): names the kernels an
+    ncu capture in profiles/ was taken on."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "trellis_quantized_weight_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
+        with open(f, encoding="utf-8") as fh:
             h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

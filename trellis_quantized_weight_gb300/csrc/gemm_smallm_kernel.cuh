@@ -15,9 +15,10 @@
 //    4*R rows and every activation value a lane loads from shared memory feeds
 //    R rows and both weights of an f32x2 FMA.
 //  * WARPS tiles form a "tile-group".  Work units are (tile-group, 256-weight
-//    block) pairs, numbered tile-group-major, and CTA c takes the contiguous
-//    unit range [c*U/P, (c+1)*U/P): every SM gets the same number of weights
-//    whatever N and K are (stream-K split).  All warps of a CTA walk the same
+//    block) pairs, numbered tile-group-major, and CTA c takes a contiguous
+//    range of floor(U/P) units, one more if c < U mod P: every SM gets the
+//    same number of weights, to one unit, whatever N and K are (stream-K
+//    split).  All warps of a CTA walk the same
 //    blocks in step, so the CTA stages x UB blocks ahead, as fp32, through a
 //    2*UB-slot shared-memory ring ([group][m][32 k], groups padded by 16 bytes
 //    so the 8 groups of a load hit 8 different bank quads), with one CTA
@@ -82,11 +83,15 @@ struct SmallMCfg {
     static constexpr size_t SMEM_BYTES = TABLE_BYTES + RING * XS_UNIT * sizeof(float);
 };
 
-// The shape used by the library for each M (chosen by timing the M = 1, 5, 8
-// and 15 workloads on GB300 over R, WARPS, LUT and CTAs per SM).
+// The shape used by the library for each M, chosen by timing back-to-back
+// calls of the M = 1, 5, 8 and 15 workloads on GB300 over R, WARPS, UB, LUT and
+// CTAs per SM (M in between takes its neighbours' shape).
 template <int MM>
 struct SmallMDefault {
-    using type = SmallMCfg<MM, (MM <= 5) ? 4 : 3, (MM <= 7) ? 16 : (MM <= 11 ? 12 : 8), true>;
+    static constexpr int WARPS = (MM <= 7) ? 16 : (MM <= 11 ? 12 : 8);
+    static constexpr int UB = (MM <= 2) ? 3 : (MM <= 5) ? 4 : (MM <= 11) ? 2 : 3;
+    using type = SmallMCfg<MM, 3, WARPS, true, 1, UB>;
+    static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
 
 __device__ __forceinline__ int unit_begin(int c, const SmallMPlan& p) {
