@@ -281,7 +281,12 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     uint32_t cw[R][KB];
     int tg = -1, row0 = 0, tile = 0, b_first = 0;
     bool live = false;
-    auto begin_segment = [&]() {
+    // Scales of the next segment: requested, with its first block of codes,
+    // during the current segment's last unit.
+    float snext[R];
+    // A segment starts at unit (utg, b).  Its first codes and scales are loaded
+    // here, or were already requested one unit ahead (prefetched).
+    auto begin_segment = [&](bool prefetched) {
         tg = utg;
         b_first = b;
         tile = tg * WARPS + warp;
@@ -291,22 +296,44 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         for (int r = 0; r < R; ++r) {
             const int n = row0 + slot + 4 * r;
             ok[r] = n < p.N;
-            const float sr = ok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
+            float sr;
+            if (prefetched)
+                sr = snext[r];
+            else
+                sr = ok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
             s2[r] = make_float2(sr, sr);
             rp[r] = codes + static_cast<size_t>(ok[r] ? n : 0) * p.row_words;
 #pragma unroll
             for (int m = 0; m < MM; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
         }
-        if (live) load_block_group<KB, R>(rp, ok, b, g, cw);
+        if (live && !prefetched) load_block_group<KB, R>(rp, ok, b, g, cw);
     };
 
     // Shared-memory set-up first: under a programmatic launch it overlaps the
-    // previous kernel's tail.  No global memory is read or written before
-    // griddep_wait().  Then the first segment's codes and the x of the first
-    // UB units (into ring slots 0 .. UB-1).
+    // previous kernel's tail, together with L2 prefetches of the first unit's
+    // codes and x (L2 is coherent, so these cannot observe stale data).
+    // Nothing is loaded into registers or written before griddep_wait().  Then
+    // the first segment's codes and the x of the first UB units (into ring
+    // slots 0 .. UB-1).
+    if (nunits > 0) {
+        const int prow0 = (utg * WARPS + warp) * C::ROWS_PER_TILE;
+        if (g == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int n = prow0 + slot + 4 * r;
+                if (n < p.N)
+                    asm volatile("prefetch.global.L2 [%0];"
+                                 :: "l"(codes + static_cast<size_t>(n) * p.row_words + b * (kGroupsPerBlock * KB)));
+            }
+        }
+        // x of the first unit: MM rows of 512 bytes, 4 lines each
+        if (tid < MM * 4)
+            asm volatile("prefetch.global.L2 [%0];"
+                         :: "l"(x + static_cast<size_t>(tid >> 2) * p.K + b * 256 + (tid & 3) * 64));
+    }
     if constexpr (C::LUT) build_quotient_table(reinterpret_cast<float*>(smem_raw), tid, NT);
     griddep_wait();
-    if (nunits > 0) begin_segment();
+    if (nunits > 0) begin_segment(false);
     {
         uint4 xfirst[UB][C::XPT];
 #pragma unroll
@@ -350,7 +377,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 }
         }
 
-        if (seg_start && rel > 0) begin_segment();
+        if (seg_start && rel > 0) begin_segment(true);
 
         if (live) {
             // the block after next: pull it toward L2 now, so the register
@@ -364,6 +391,20 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             uint32_t nw[R][KB];
             if (!seg_end) {
                 load_block_group<KB, R>(rp, ok, b + 1, g, nw);
+            } else if (rel + 1 < nunits) {
+                // the next unit starts tile-group utg + 1 at block 0: request
+                // its codes and scales now
+                const int nrow0 = ((utg + 1) * WARPS + warp) * C::ROWS_PER_TILE;
+                bool nok[R];
+                const uint32_t* nrp[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int n = nrow0 + slot + 4 * r;
+                    nok[r] = n < p.N;
+                    nrp[r] = codes + static_cast<size_t>(nok[r] ? n : 0) * p.row_words;
+                    snext[r] = nok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
+                }
+                load_block_group<KB, R>(nrp, nok, 0, g, nw);
             } else {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
