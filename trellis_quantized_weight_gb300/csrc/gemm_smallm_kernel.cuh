@@ -88,8 +88,8 @@ struct SmallMCfg {
 // CTAs per SM (M in between takes its neighbours' shape).
 template <int MM>
 struct SmallMDefault {
-    static constexpr int WARPS = (MM <= 7) ? 16 : (MM <= 11 ? 12 : 8);
-    static constexpr int UB = (MM <= 2) ? 3 : (MM <= 5) ? 4 : (MM <= 11) ? 2 : 3;
+    static constexpr int WARPS = (MM <= 2) ? 16 : (MM <= 11 ? 12 : 8);
+    static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
     using type = SmallMCfg<MM, 3, WARPS, true, 1, UB>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
@@ -254,9 +254,9 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                    const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, SmallMPlan p) {
     constexpr int MM = C::MM, R = C::R, WARPS = C::WARPS, XG = C::XG, XS_UNIT = C::XS_UNIT;
     constexpr int NT = C::NT;
-    constexpr int UB = C::UB, RING = C::RING;
+    constexpr int UB = C::UB;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float* xs = reinterpret_cast<float*>(smem_raw + C::TABLE_BYTES);   // RING slots of XS_UNIT floats
+    float* xs = reinterpret_cast<float*>(smem_raw + C::TABLE_BYTES);   // C::RING slots of XS_UNIT floats
 
     const int c = blockIdx.x;
     const int u0 = unit_begin(c, p);
@@ -360,12 +360,13 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     bool pend0 = false, pend1 = false;
     int ptg0 = 0, ptg1 = 0;
 
+    int ph = 0, rhalf = 0;   // position in the current phase of UB units; ring half it uses
     for (int rel = 0; rel < nunits; ++rel) {
-        const int ring = rel % RING;
+        const int ring = rhalf * UB + ph;   // ring slot of this unit's x
         const bool seg_start = (rel == 0) || (b == 0);
         const bool seg_end = (rel + 1 == nunits) || (b + 1 == p.nblocks);
-        const bool phase_start = (rel % UB) == 0;
-        const bool phase_end = (rel % UB) == UB - 1 || rel + 1 == nunits;
+        const bool phase_start = ph == 0;
+        const bool phase_end = ph == UB - 1 || rel + 1 == nunits;
 
         if (phase_start) {
 #pragma unroll
@@ -502,17 +503,20 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         }
 
         if (phase_end) {
-            const int pbase = rel - (rel % UB);
+            // the next phase's units use the other half of the ring
+            const int pbase = rel - ph;
 #pragma unroll
-            for (int j = 0; j < UB; ++j) {
-                const int rn = pbase + UB + j;
-                if (rn < nunits) x_block_store<C>(xs + (rn % RING) * XS_UNIT, tid, xnext[j]);
-            }
+            for (int j = 0; j < UB; ++j)
+                if (pbase + UB + j < nunits) x_block_store<C>(xs + ((rhalf ^ 1) * UB + j) * XS_UNIT, tid, xnext[j]);
             __syncthreads();
         }
         if (++b == p.nblocks) {
             b = 0;
             ++utg;
+        }
+        if (++ph == UB) {
+            ph = 0;
+            rhalf ^= 1;
         }
     }
 

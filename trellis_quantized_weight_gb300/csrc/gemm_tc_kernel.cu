@@ -50,19 +50,13 @@ constexpr int kTcTmaWarp = kTcDecodeWarps;
 constexpr int kTcMmaWarp = kTcDecodeWarps + 1;
 constexpr int kTcTmemCols = 64;
 
-// Over all 4096 windows of 12 bits the byte sum S of the hash spans [62, 964]
-// (codes -448 .. 454), so the table keeps only those 903 entries.
-constexpr int kSumLo = 62;
-constexpr int kSumHi = 964;
-constexpr int kTableEntries = kSumHi - kSumLo + 1;
-constexpr int kTableBytes = kTableEntries * 32 * 4;                  // 115,584
 // Quotient by the per-lane table (one shared load) or by the three-op
 // residual correction (ALU only).  This kernel's shared-memory pipe is busy
 // with the A tiles, the activation tiles and the tensor cores' operand reads,
 // while its issue slots are not, so the ALU form is used and the table's
 // shared memory goes to deeper pipelining instead.
 constexpr bool kTcLut = false;
-constexpr int kTableRegion = kTcLut ? (kTableBytes + 1023) / 1024 * 1024 : 0;
+constexpr int kTableRegion = kTcLut ? (kQuotientTableBytes + 1023) / 1024 * 1024 : 0;
 
 constexpr int kABytes = kTcRows * kTcStageK * 2;     // 32 KB
 constexpr int kBBytes = kTcM * kTcStageK * 2;        // 16 KB
@@ -201,13 +195,7 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (kTcLut && warp < kTcDecodeWarps) {
-        // quotient table for S in [62, 964], one copy per lane
-        float* table = reinterpret_cast<float*>(smem);
-        for (int e = threadIdx.x; e < kTableEntries * 8; e += kTcDecodeWarps * 32) {
-            const int si = e >> 3, quad = e & 7;
-            const float v = code_to_value(static_cast<float>(si + kSumLo - 510));
-            *reinterpret_cast<float4*>(table + si * 32 + quad * 4) = make_float4(v, v, v, v);
-        }
+        build_quotient_table(reinterpret_cast<float*>(smem), threadIdx.x, kTcDecodeWarps * 32);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -225,7 +213,7 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         const float sr = ok ? bf16_bits_to_f32(__ldg(scales + row)) : 0.0f;
         const float2 s2 = make_float2(sr, sr);
         const uint32_t* row_codes = codes + static_cast<size_t>(ok ? row : 0) * row_words;
-        const uint32_t lane_tbl = sbase + 4u * static_cast<uint32_t>(lane) - static_cast<uint32_t>(kSumLo * 128);
+        const uint32_t lane_tbl = quotient_table_lane_address(smem, lane);
         const int src_lane = (gi == 0) ? lane : lane - 8;
         // this thread's 4 core-matrix rows inside a stage's A tile
         const uint32_t a_row_off = static_cast<uint32_t>((row_local >> 3) * kCoreSBO + gi * 4 * kCoreLBO +

@@ -76,24 +76,30 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // ---- quotient table ---------------------------------------------------------
-// The value depends on the window only through the byte sum S = code + 510,
-// S in [0, 1020].  A shared-memory table holds value(S) once per lane:
-// entry (S, lane) sits at byte 128*S + 4*lane, so the 32 lanes of a warp always
-// read 32 different banks, whatever their S.  dp4a(z, 0x80808080, base) yields
-// base + 128*S directly, so a lookup is one dp4a and one shared load.
-constexpr int kByteSums = 1021;
-constexpr int kQuotientTableBytes = kByteSums * 32 * 4;   // 130,688 bytes
+// The value depends on the window only through the byte sum S = code + 510 of
+// its hash.  Over the 4096 12-bit windows S only takes values in [62, 964]
+// (the host tests enumerate them), so a shared-memory table holds value(S)
+// for those 903 sums, once per lane: entry (S, lane) sits at byte
+// 128*(S - 62) + 4*lane, and the 32 lanes of a warp always read 32 different
+// banks, whatever their S.  dp4a(z, 0x80808080, base) yields base + 128*S
+// directly (base = the lane's entry address minus 128*62, in wrapping 32-bit
+// arithmetic), so a lookup is one dp4a and one shared load.
+constexpr int kSumLo = 62;
+constexpr int kSumHi = 964;
+constexpr int kTableSums = kSumHi - kSumLo + 1;                  // 903
+constexpr int kQuotientTableBytes = kTableSums * 32 * 4;        // 115,584 bytes
 
 __device__ __forceinline__ void build_quotient_table(float* table, int tid, int nthreads) {
-    for (int e = tid; e < kByteSums * 8; e += nthreads) {
-        const int sum = e >> 3, quad = e & 7;
-        const float v = code_to_value(static_cast<float>(sum - 510));
-        *reinterpret_cast<float4*>(table + sum * 32 + quad * 4) = make_float4(v, v, v, v);
+    for (int e = tid; e < kTableSums * 8; e += nthreads) {
+        const int si = e >> 3, quad = e & 7;
+        const float v = code_to_value(static_cast<float>(si + kSumLo - 510));
+        *reinterpret_cast<float4*>(table + si * 32 + quad * 4) = make_float4(v, v, v, v);
     }
 }
 
 __device__ __forceinline__ uint32_t quotient_table_lane_address(const void* table, int lane) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(table)) + 4u * static_cast<uint32_t>(lane);
+    return static_cast<uint32_t>(__cvta_generic_to_shared(table)) + 4u * static_cast<uint32_t>(lane) -
+           static_cast<uint32_t>(kSumLo * 128);
 }
 
 __device__ __forceinline__ float quotient_lookup(uint32_t win, uint32_t lane_address) {
