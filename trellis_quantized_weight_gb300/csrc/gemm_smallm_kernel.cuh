@@ -55,6 +55,8 @@ struct SmallMPlan {
     int P;              // CTAs
     int U;              // units = ntg * nblocks (below 2^31: N*K/256 is)
     int base, rem;      // CTA c takes base + (c < rem) units, c*base + min(c, rem) first
+    FastDiv div_base1;  // division by base + 1
+    FastDiv div_base;   // division by base
     float* partials;    // workspace: [P][2][WARPS][R*M*4] fp32
     uint32_t* counters; // workspace: [ntg * WARPS]
 };
@@ -100,7 +102,8 @@ __device__ __forceinline__ int unit_begin(int c, const SmallMPlan& p) {
 
 __device__ __forceinline__ int cta_of_unit(int u, const SmallMPlan& p) {
     const int big = p.rem * (p.base + 1);   // units of the CTAs that take base + 1
-    return u < big ? u / (p.base + 1) : p.rem + (u - big) / p.base;
+    return u < big ? static_cast<int>(p.div_base1.div(static_cast<uint32_t>(u)))
+                   : p.rem + static_cast<int>(p.div_base.div(static_cast<uint32_t>(u - big)));
 }
 
 // A tile's ticket: add 1 to its counter at GPU scope with release semantics
@@ -569,6 +572,8 @@ SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev) {
     p.P = P;
     p.base = p.U / P;
     p.rem = p.U % P;
+    p.div_base1 = FastDiv(static_cast<uint32_t>(p.base + 1));
+    p.div_base = FastDiv(static_cast<uint32_t>(p.base));
     return p;
 }
 
