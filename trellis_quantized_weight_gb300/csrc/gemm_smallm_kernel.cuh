@@ -180,13 +180,32 @@ __device__ __forceinline__ void x_block_store(float* slot, int tid, const uint4 
     }
 }
 
+// The CTAs that contribute to a tile-group, packed in one word: the first
+// (bits 0-14) and the last (bits 15-29) contributing CTA, and bit 30 set when
+// the first one keeps its partial sums in slot 1 (its range starts before the
+// tile-group: every CTA after the first starts inside the tile-group, so the
+// tile-group is its first, slot 0).  Computed when a segment starts, off the
+// critical path at the end of the kernel.
+__device__ __forceinline__ uint32_t contributors_info(int tg, const SmallMPlan& p) {
+    const int tg_u0 = tg * p.nblocks;
+    const int c_first = cta_of_unit(tg_u0, p);
+    const int c_last = cta_of_unit(tg_u0 + p.nblocks - 1, p);
+    const uint32_t slot1 = unit_begin(c_first, p) < tg_u0 ? 1u : 0u;
+    return static_cast<uint32_t>(c_first) | (static_cast<uint32_t>(c_last) << 15) | (slot1 << 30);
+}
+__device__ __forceinline__ int info_first(uint32_t info) { return static_cast<int>(info & 0x7FFFu); }
+__device__ __forceinline__ int info_last(uint32_t info) { return static_cast<int>((info >> 15) & 0x7FFFu); }
+__device__ __forceinline__ int info_slot(uint32_t info) { return static_cast<int>(info >> 30); }
+
 // Adds the partial sums of up to two split tiles of this warp (tile-groups
-// tgs[t] where use[t]) in CTA order, rounds to bf16, stores, and resets the
-// tiles' counters.  All loads of a round, for both tiles, are issued before
-// the first add, so the reduction costs one round trip per 8 contributors.
+// tgs[t] where use[t], contributors infos[t]) in CTA order, rounds to bf16,
+// stores, and resets the tiles' counters.  All loads of a round, for both
+// tiles, are issued before the first add, so the reduction costs one round
+// trip per 8 contributors.
 template <class C>
 __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bool (&use)[2], const int (&tgs)[2],
-                                                   int warp, int lane, uint16_t* __restrict__ out) {
+                                                   const uint32_t (&infos)[2], int warp, int lane,
+                                                   uint16_t* __restrict__ out) {
     constexpr int MM = C::MM, WARPS = C::WARPS;
     constexpr int E = C::R * MM * 4;                  // sums of one warp's tile
     constexpr int EP = (E + 31) / 32;                 // sums per lane
@@ -194,13 +213,9 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
     int rounds = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        const int tg_u0 = tgs[t] * p.nblocks;
-        c_first[t] = use[t] ? cta_of_unit(tg_u0, p) : 1;
-        c_last[t] = use[t] ? cta_of_unit(tg_u0 + p.nblocks - 1, p) : 0;
-        // Every CTA after c_first starts inside the tile-group, so the
-        // tile-group is its first (slot 0); c_first used slot 1 unless its
-        // range also starts at the tile-group's first unit.
-        cf_slot[t] = (use[t] && unit_begin(c_first[t], p) < tg_u0) ? 1 : 0;
+        c_first[t] = use[t] ? info_first(infos[t]) : 1;
+        c_last[t] = use[t] ? info_last(infos[t]) : 0;
+        cf_slot[t] = use[t] ? info_slot(infos[t]) : 0;
         const int r = (c_last[t] - c_first[t] + 8) >> 3;
         rounds = r > rounds ? r : rounds;
     }
@@ -289,9 +304,11 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     float snext[R];
     // A segment starts at unit (utg, b).  Its first codes and scales are loaded
     // here, or were already requested one unit ahead (prefetched).
+    uint32_t seg_info = 0;   // contributors of the current segment's tile-group
     auto begin_segment = [&](bool prefetched) {
         tg = utg;
         b_first = b;
+        seg_info = contributors_info(tg, p);
         tile = tg * WARPS + warp;
         row0 = tile * C::ROWS_PER_TILE;
         live = row0 < p.N;   // whole tile beyond N: skipped by every CTA alike
@@ -362,6 +379,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     // no fence or atomic round trip stalls the loop.  Indexed by partial slot.
     bool pend0 = false, pend1 = false;
     int ptg0 = 0, ptg1 = 0;
+    uint32_t pinfo0 = 0, pinfo1 = 0;
 
     int ph = 0, rhalf = 0;   // position in the current phase of UB units; ring half it uses
     for (int rel = 0; rel < nunits; ++rel) {
@@ -498,9 +516,11 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 if (pslot == 0) {
                     pend0 = true;
                     ptg0 = tg;
+                    pinfo0 = seg_info;
                 } else {
                     pend1 = true;
                     ptg1 = tg;
+                    pinfo1 = seg_info;
                 }
             }
         }
@@ -537,14 +557,11 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         t0 = __shfl_sync(0xffffffffu, t0, 0);
         t1 = __shfl_sync(0xffffffffu, t1, 0);
         __syncwarp();   // every lane's loads below are ordered after lane 0's acquire
-        auto contributors = [&](int t) {
-            const int tg_u0 = t * p.nblocks;
-            return cta_of_unit(tg_u0 + p.nblocks - 1, p) - cta_of_unit(tg_u0, p) + 1;
-        };
-        const bool use[2] = {pend0 && t0 == static_cast<uint32_t>(contributors(ptg0) - 1),
-                             pend1 && t1 == static_cast<uint32_t>(contributors(ptg1) - 1)};
+        const bool use[2] = {pend0 && t0 == static_cast<uint32_t>(info_last(pinfo0) - info_first(pinfo0)),
+                             pend1 && t1 == static_cast<uint32_t>(info_last(pinfo1) - info_first(pinfo1))};
         const int tgs[2] = {ptg0, ptg1};
-        if (use[0] || use[1]) reduce_split_tiles<C>(p, use, tgs, warp, lane, out);
+        const uint32_t infos[2] = {pinfo0, pinfo1};
+        if (use[0] || use[1]) reduce_split_tiles<C>(p, use, tgs, infos, warp, lane, out);
     }
 }
 
@@ -594,6 +611,7 @@ int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint1
                            cudaStream_t stream, const DeviceInfo& dev) {
     SmallMPlan p = plan_smallm<C>(K, N, KB, dev);
     if (!smallm_fits_counters<C>(p)) return -2;
+    if (p.P >= (1 << 15)) return -3;   // CTA indices are packed in 15 bits (contributors_info)
     const size_t need = smallm_workspace_bytes<C>(p);
     if (ws_bytes < need || ws == nullptr) return -7;
     p.counters = static_cast<uint32_t*>(ws);
