@@ -6,11 +6,16 @@
 // once and share it across every activation row).
 //
 // Mapping (GB300-first, not the page's simdgroup layout):
-//  * A warp's 32 lanes are 4 row slots x 8 groups: lane l decodes group
-//    g = l%8 (32 weights) of the rows held by slot q = l/8.  The 8 lanes of a
-//    slot read one row's 32*k-byte block together, so a warp-wide code load
-//    touches 4 cache lines, and the lookahead word of group g (the first word
-//    of group g-1, or word 0 of the block for g = 0) arrives by one shuffle.
+//  * A warp's 32 lanes are 4 row slots x 8 groups: the lane decodes group g
+//    (32 weights) of the rows held by its slot q.  The 8 lanes of a slot read
+//    one row's 32*k-byte block together, so a warp-wide code load touches 4
+//    cache lines, and the lookahead word of group g (the first word of group
+//    g-1, or word 0 of the block for g = 0) arrives by one shuffle.  Lane order
+//    is a per-shape choice: slot-major (l = 8q + g: each quarter-warp's code
+//    load is one row's contiguous block) or group-major (l = 4g + q: the 4
+//    slots reading the same activations are adjacent, which serves a 16-byte
+//    shared load in 2 wavefronts instead of 4, but spreads a quarter-warp's
+//    code load over 4 rows).
 //  * Each lane holds R rows (slot q: rows q, q+4, ...), so a warp's tile is
 //    4*R rows and every activation value a lane loads from shared memory feeds
 //    R rows and both weights of an f32x2 FMA.
@@ -24,7 +29,7 @@
 //    so the 8 groups of a load hit 8 different bank quads), with one CTA
 //    barrier per UB blocks.
 //  * At the end of a row segment the 8 lanes of a slot add their per-group
-//    sums by butterfly shuffles.  A row whose K-range is split over several
+//    sums by butterfly shuffles (lane distances 4, 8, 16).  A row whose K-range is split over several
 //    CTAs writes fp32 partial sums to the workspace as soon as its segment
 //    ends; only a CTA's first and last segments can be split, and both take
 //    their per-tile tickets after the CTA's last unit, so the loop never waits
@@ -66,7 +71,10 @@ struct SmallMPlan {
 //   WARPS  warps per CTA (= tiles per tile-group)
 //   LUT    decode the quotient through a shared-memory table instead of the
 //          three-op residual correction (same bits either way)
-template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1, int UB_ = 2>
+//   OCC    CTAs per SM
+//   UB     blocks staged per CTA barrier
+//   GM     group-major lane order (see the mapping notes above)
+template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1, int UB_ = 2, bool GM_ = false>
 struct SmallMCfg {
     static constexpr int MM = MM_;
     static constexpr int R = R_;
@@ -83,6 +91,8 @@ struct SmallMCfg {
     static constexpr int UB = UB_;                                // blocks per CTA barrier
     static constexpr int RING = 2 * UB;                           // x ring slots
     static constexpr size_t SMEM_BYTES = TABLE_BYTES + RING * XS_UNIT * sizeof(float);
+    static constexpr bool GM = GM_;
+    static constexpr int GROUP_STRIDE = GM ? 4 : 1;  // lane distance between groups of a slot
 };
 
 // The shape used by the library for each M, chosen by timing back-to-back
@@ -92,7 +102,8 @@ template <int MM>
 struct SmallMDefault {
     static constexpr int WARPS = (MM <= 2) ? 16 : (MM <= 11 ? 12 : 8);
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
-    using type = SmallMCfg<MM, 3, WARPS, true, 1, UB>;
+    static constexpr bool GM = MM >= 6 && MM <= 11;   // activation traffic outweighs code traffic
+    using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
 
@@ -281,8 +292,10 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     const int u1 = unit_begin(c + 1, p);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int g = lane & 7, slot = lane >> 3;
-    const int src_lane = (g == 0) ? lane + 7 : lane - 1;
+    const int g = C::GM ? lane >> 2 : lane & 7;
+    const int slot = C::GM ? lane & 3 : lane >> 3;
+    // the lane of the same slot holding group g - 1 (mod 8)
+    const int src_lane = (g == 0) ? lane + 7 * C::GROUP_STRIDE : lane - C::GROUP_STRIDE;
     const int first_tg = u0 / p.nblocks;
 
     // (tile-group, block) of the current unit, advanced incrementally: no
@@ -486,9 +499,9 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 #pragma unroll
                 for (int m = 0; m < MM; ++m) {
                     float t = __fadd_rn(acc[r][m].x, acc[r][m].y);
-                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 1));
-                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 2));
-                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 4));
+                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, C::GROUP_STRIDE));       // group g ^ 1
+                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 2 * C::GROUP_STRIDE));   // group g ^ 2
+                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 4 * C::GROUP_STRIDE));   // group g ^ 4
                     v[r][m] = t;   // identical in the 8 lanes of the slot
                 }
 
