@@ -11,11 +11,12 @@
 //    one row's 32*k-byte block together, so a warp-wide code load touches 4
 //    cache lines, and the lookahead word of group g (the first word of group
 //    g-1, or word 0 of the block for g = 0) arrives by one shuffle.  Lane order
-//    is a per-shape choice: slot-major (l = 8q + g: each quarter-warp's code
-//    load is one row's contiguous block) or group-major (l = 4g + q: the 4
-//    slots reading the same activations are adjacent, which serves a 16-byte
-//    shared load in 2 wavefronts instead of 4, but spreads a quarter-warp's
-//    code load over 4 rows).
+//    is a per-shape choice: slot-major (l = 8q + g) or group-major
+//    (l = 4g + q: the 4 slots reading the same activations are adjacent, which
+//    serves a 16-byte shared load in 2 wavefronts instead of 4).  Codes are
+//    always loaded slot-major, each quarter-warp reading one row's contiguous
+//    block; in group-major order k + 1 shuffles per row and block then hand
+//    each lane its group's words and the lookahead word.
 //  * Each lane holds R rows (slot q: rows q, q+4, ...), so a warp's tile is
 //    4*R rows and every activation value a lane loads from shared memory feeds
 //    R rows and both weights of an f32x2 FMA.
@@ -102,7 +103,7 @@ template <int MM>
 struct SmallMDefault {
     static constexpr int WARPS = (MM <= 2) ? 16 : (MM <= 11 ? 12 : 8);
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
-    static constexpr bool GM = MM >= 6 && MM <= 11;   // activation traffic outweighs code traffic
+    static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
     using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
@@ -296,6 +297,10 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     const int slot = C::GM ? lane & 3 : lane >> 3;
     // the lane of the same slot holding group g - 1 (mod 8)
     const int src_lane = (g == 0) ? lane + 7 * C::GROUP_STRIDE : lane - C::GROUP_STRIDE;
+    // Code loads are always slot-major (each quarter-warp reads one row's
+    // contiguous block): this lane loads group lg of the rows of slot lslot.
+    // In group-major order the words then move to their lane by shuffles.
+    const int lslot = lane >> 3, lg = lane & 7;
     const int first_tg = u0 / p.nblocks;
 
     // (tile-group, block) of the current unit, advanced incrementally: no
@@ -327,19 +332,20 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         live = row0 < p.N;   // whole tile beyond N: skipped by every CTA alike
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int n = row0 + slot + 4 * r;
-            ok[r] = n < p.N;
+            const int n = row0 + slot + 4 * r;    // this lane's row
+            const int nl = row0 + lslot + 4 * r;  // the row this lane loads codes for
+            ok[r] = nl < p.N;
             float sr;
             if (prefetched)
                 sr = snext[r];
             else
-                sr = ok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
+                sr = n < p.N ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
             s2[r] = make_float2(sr, sr);
-            rp[r] = codes + static_cast<size_t>(ok[r] ? n : 0) * p.row_words;
+            rp[r] = codes + static_cast<size_t>(ok[r] ? nl : 0) * p.row_words;
 #pragma unroll
             for (int m = 0; m < MM; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
         }
-        if (live && !prefetched) load_block_group<KB, R>(rp, ok, b, g, cw);
+        if (live && !prefetched) load_block_group<KB, R>(rp, ok, b, lg, cw);
     };
 
     // Shared-memory set-up first: under a programmatic launch it overlaps the
@@ -350,10 +356,10 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     // slots 0 .. UB-1).
     if (nunits > 0) {
         const int prow0 = (utg * WARPS + warp) * C::ROWS_PER_TILE;
-        if (g == 0) {
+        if (lg == 0) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const int n = prow0 + slot + 4 * r;
+                const int n = prow0 + lslot + 4 * r;
                 if (n < p.N)
                     asm volatile("prefetch.global.L2 [%0];"
                                  :: "l"(codes + static_cast<size_t>(n) * p.row_words + b * (kGroupsPerBlock * KB)));
@@ -420,12 +426,12 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             if (b + 2 < p.nblocks && rel + 2 < nunits) {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    if (ok[r] && g == 0)
+                    if (ok[r] && lg == 0)
                         asm volatile("prefetch.global.L2 [%0];" :: "l"(rp[r] + (b + 2) * (kGroupsPerBlock * KB)));
             }
             uint32_t nw[R][KB];
             if (!seg_end) {
-                load_block_group<KB, R>(rp, ok, b + 1, g, nw);
+                load_block_group<KB, R>(rp, ok, b + 1, lg, nw);
             } else if (rel + 1 < nunits) {
                 // the next unit starts tile-group utg + 1 at block 0: request
                 // its codes and scales now
@@ -435,11 +441,12 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     const int n = nrow0 + slot + 4 * r;
-                    nok[r] = n < p.N;
-                    nrp[r] = codes + static_cast<size_t>(nok[r] ? n : 0) * p.row_words;
-                    snext[r] = nok[r] ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
+                    const int nl = nrow0 + lslot + 4 * r;
+                    nok[r] = nl < p.N;
+                    nrp[r] = codes + static_cast<size_t>(nok[r] ? nl : 0) * p.row_words;
+                    snext[r] = n < p.N ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
                 }
-                load_block_group<KB, R>(nrp, nok, 0, g, nw);
+                load_block_group<KB, R>(nrp, nok, 0, lg, nw);
             } else {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
@@ -447,11 +454,23 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                     for (int i = 0; i < KB; ++i) nw[r][i] = 0u;
             }
             uint32_t w[R][KB + 1];
+            if constexpr (C::GM) {
+                // group g of slot's row was loaded by lane 8*slot + g; the
+                // lookahead is group g - 1's first word
+                const int from = 8 * slot + g, from_prev = 8 * slot + ((g + 7) & 7);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
+                for (int r = 0; r < R; ++r) {
 #pragma unroll
-                for (int i = 0; i < KB; ++i) w[r][i] = cw[r][i];
-                w[r][KB] = __shfl_sync(0xffffffffu, cw[r][0], src_lane);
+                    for (int i = 0; i < KB; ++i) w[r][i] = __shfl_sync(0xffffffffu, cw[r][i], from);
+                    w[r][KB] = __shfl_sync(0xffffffffu, cw[r][0], from_prev);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+#pragma unroll
+                    for (int i = 0; i < KB; ++i) w[r][i] = cw[r][i];
+                    w[r][KB] = __shfl_sync(0xffffffffu, cw[r][0], src_lane);
+                }
             }
             const float* xq = xs + ring * XS_UNIT + g * XG;
 #pragma unroll
@@ -510,7 +529,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 // slot stores the outputs m with m % 8 == g
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    if (ok[r])
+                    if (row0 + slot + 4 * r < p.N)
 #pragma unroll
                         for (int m = 0; m < MM; ++m)
                             if ((m & 7) == g)
