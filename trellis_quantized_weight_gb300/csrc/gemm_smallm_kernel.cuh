@@ -512,38 +512,48 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 
         if (live && seg_end) {
             // ---- per-row sums: k-pair halves, then the 8 groups of the slot ----
-            float v[R][MM];
+            // Transposing butterfly over the slot's 8 lanes: each step adds
+            // the partner's half of the values and keeps half as many, so
+            // after three steps lane g holds the complete sums of the NV/8
+            // values starting at vbase (the same pairwise sums as a plain
+            // butterfly, in a third of the shuffles).  Value i = r*MM + m.
+            constexpr int NV = (R * MM + 7) / 8 * 8;
+            float v[NV];
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+            for (int i = 0; i < NV; ++i)
+                v[i] = (i < R * MM) ? __fadd_rn(acc[i / MM][i % MM].x, acc[i / MM][i % MM].y) : 0.0f;
+            int vbase = 0;
 #pragma unroll
-                for (int m = 0; m < MM; ++m) {
-                    float t = __fadd_rn(acc[r][m].x, acc[r][m].y);
-                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, C::GROUP_STRIDE));       // group g ^ 1
-                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 2 * C::GROUP_STRIDE));   // group g ^ 2
-                    t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, 4 * C::GROUP_STRIDE));   // group g ^ 4
-                    v[r][m] = t;   // identical in the 8 lanes of the slot
+            for (int step = 0; step < 3; ++step) {
+                const int h = NV >> (step + 1);              // values kept after this step
+                const bool upper = (g >> step) & 1;         // this lane keeps the upper half
+#pragma unroll
+                for (int i = 0; i < h; ++i) {
+                    const float lo = v[i], hi = v[i + h];
+                    const float other = __shfl_xor_sync(0xffffffffu, upper ? lo : hi, C::GROUP_STRIDE << step);
+                    v[i] = __fadd_rn(upper ? hi : lo, other);
                 }
+                vbase += upper ? h : 0;
+            }
 
             if (b_first == 0 && b + 1 == p.nblocks) {
-                // this CTA owns the whole K-range of the tile-group; lane g of a
-                // slot stores the outputs m with m % 8 == g
+                // this CTA owns the whole K-range of the tile-group
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-                    if (row0 + slot + 4 * r < p.N)
-#pragma unroll
-                        for (int m = 0; m < MM; ++m)
-                            if ((m & 7) == g)
-                                out[static_cast<size_t>(m) * p.N + row0 + slot + 4 * r] = bf16_bits_rn(v[r][m]);
+                for (int j = 0; j < NV / 8; ++j) {
+                    const int i = vbase + j;
+                    const int r = i / MM, m = i - r * MM;
+                    if (i < R * MM && row0 + slot + 4 * r < p.N)
+                        out[static_cast<size_t>(m) * p.N + row0 + slot + 4 * r] = bf16_bits_rn(v[j]);
+                }
             } else {
                 // ---- split row: publish the partial now, take the ticket after the loop ----
-                // element (r, m) of row slot q sits at [(r*MM + m)*4 + q]; lane g == 0 writes
+                // value (r, m) of row slot q sits at [(r*MM + m)*4 + q]
                 const int pslot = (tg == first_tg) ? 0 : 1;
                 float* mine = p.partials + ((static_cast<size_t>(c) * 2 + pslot) * WARPS + warp) * (R * MM * 4);
-                if (g == 0) {
 #pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int m = 0; m < MM; ++m) mine[(r * MM + m) * 4 + slot] = v[r][m];
+                for (int j = 0; j < NV / 8; ++j) {
+                    const int i = vbase + j;
+                    if (i < R * MM) mine[i * 4 + slot] = v[j];
                 }
                 if (pslot == 0) {
                     pend0 = true;
