@@ -75,7 +75,14 @@ struct SmallMPlan {
 //   OCC    CTAs per SM
 //   UB     blocks staged per CTA barrier
 //   GM     group-major lane order (see the mapping notes above)
-template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1, int UB_ = 2, bool GM_ = false>
+//   ET     early tickets: a split segment that ends before the CTA's last
+//          unit takes its ticket inside the loop, and the segment that runs
+//          to the last unit skips its ticket when the counter it read at its
+//          start shows every other contributor done.  Pays when every CTA's
+//          range spans a tile-group boundary (each split tile then has two
+//          contributors, one finishing early); the in-loop fence costs more
+//          than it saves otherwise.
+template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1, int UB_ = 2, bool GM_ = false, bool ET_ = false>
 struct SmallMCfg {
     static constexpr int MM = MM_;
     static constexpr int R = R_;
@@ -93,6 +100,7 @@ struct SmallMCfg {
     static constexpr int RING = 2 * UB;                           // x ring slots
     static constexpr size_t SMEM_BYTES = TABLE_BYTES + RING * XS_UNIT * sizeof(float);
     static constexpr bool GM = GM_;
+    static constexpr bool ET = ET_;
     static constexpr int GROUP_STRIDE = GM ? 4 : 1;  // lane distance between groups of a slot
 };
 
@@ -104,7 +112,8 @@ struct SmallMDefault {
     static constexpr int WARPS = (MM <= 2) ? 16 : (MM <= 11 ? 12 : 8);
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
     static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
-    using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM>;
+    static constexpr bool ET = MM >= 12;
+    using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
 
@@ -126,6 +135,25 @@ __device__ __forceinline__ uint32_t take_ticket(uint32_t* counter) {
     uint32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
     return old;
+}
+
+// Release/acquire fence at GPU scope.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// A ticket taken inside the loop: a relaxed add after a release fence, so no
+// later load waits for its reply (the count is only read after the loop).
+__device__ __forceinline__ uint32_t take_ticket_relaxed(uint32_t* counter) {
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    return old;
+}
+
+// A counter read without ordering, issued where written; its value is used
+// after the loop, behind an acquire fence.
+__device__ __forceinline__ uint32_t load_relaxed(const uint32_t* counter) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    return v;
 }
 
 template <int KB, int R>
@@ -394,11 +422,22 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     // one CTA barrier.
     uint4 xnext[UB][C::XPT];
     // Split segments (at most two per CTA: its first and its last) publish
-    // their partial sums at once; their tickets are taken after the loop, so
-    // no fence or atomic round trip stalls the loop.  Indexed by partial slot.
+    // their partial sums at once.  Indexed by partial slot.
+    //  * A split segment that ends before the CTA's last unit takes its ticket
+    //    at the next phase end, just before the barrier, when this warp has no
+    //    loads in flight (the release fence is cheap there); the count is read
+    //    after the loop.
+    //  * The segment that runs to the CTA's last unit reads its tile's counter
+    //    when it starts.  If every other contributor had already taken its
+    //    ticket, this CTA is the last one by construction: it takes no ticket
+    //    and goes straight to the reduction after the loop.  Otherwise it takes
+    //    its ticket after the loop.
     bool pend0 = false, pend1 = false;
     int ptg0 = 0, ptg1 = 0;
     uint32_t pinfo0 = 0, pinfo1 = 0;
+    bool tk_due = false, tk_taken = false;   // slot 0's in-loop ticket
+    uint32_t tk0 = 0;                        // its previous count (lane 0)
+    uint32_t peek = 0xFFFFFFFFu;             // counter of the CTA's last segment when it started (lane 0)
 
     int ph = 0, rhalf = 0;   // position in the current phase of UB units; ring half it uses
     for (int rel = 0; rel < nunits; ++rel) {
@@ -419,6 +458,11 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         }
 
         if (seg_start && rel > 0) begin_segment(true);
+        if (C::ET && seg_start && live) {
+            const bool to_end = rel + (p.nblocks - b) >= nunits;           // runs to the CTA's last unit
+            const bool whole = b == 0 && rel + p.nblocks <= nunits;        // owns the tile-group outright
+            if (to_end && !whole && lane == 0) peek = load_relaxed(p.counters + tile);
+        }
 
         if (live) {
             // the block after next: pull it toward L2 now, so the register
@@ -559,6 +603,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                     pend0 = true;
                     ptg0 = tg;
                     pinfo0 = seg_info;
+                    tk_due = C::ET && rel + 1 < nunits;
                 } else {
                     pend1 = true;
                     ptg1 = tg;
@@ -573,6 +618,13 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 #pragma unroll
             for (int j = 0; j < UB; ++j)
                 if (pbase + UB + j < nunits) x_block_store<C>(xs + ((rhalf ^ 1) * UB + j) * XS_UNIT, tid, xnext[j]);
+            if (tk_due) {
+                __syncwarp();          // the slot lanes' partial-sum stores ...
+                fence_acq_rel_gpu();   // ... are visible before the ticket
+                if (lane == 0) tk0 = take_ticket_relaxed(p.counters + ptg0 * WARPS + warp);
+                tk_due = false;
+                tk_taken = true;
+            }
             __syncthreads();
         }
         if (++b == p.nblocks) {
@@ -588,22 +640,36 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     // the next grid on the stream may be scheduled as this CTA's SM frees up
     griddep_launch_dependents();
 
-    // ---- tickets of the split segments; the last contributor of a tile reduces it ----
+    // ---- the last contributor of a split tile reduces it ----
     if (pend0 || pend1) {
+        // The split segment that ran to the CTA's last unit, if any: slot 1,
+        // or slot 0 when it had no ticket in the loop.
+        const bool has_last = pend1 || !tk_taken;
+        const uint32_t lneed = pend1 ? static_cast<uint32_t>(info_last(pinfo1) - info_first(pinfo1))
+                                     : static_cast<uint32_t>(info_last(pinfo0) - info_first(pinfo0));
+        peek = __shfl_sync(0xffffffffu, peek, 0);
+        const bool by_peek = C::ET && has_last && peek == lneed;   // every other contributor is done
+        const bool skip0 = by_peek && !pend1;                      // slot 0 is that segment
         __syncwarp();   // the slot lanes' partial-sum stores are ordered before lane 0's tickets
-        uint32_t t0 = 0, t1 = 0;
+        uint32_t e0 = 0, e1 = 0;
         if (lane == 0) {
-            if (pend0) t0 = take_ticket(p.counters + ptg0 * WARPS + warp);
-            if (pend1) t1 = take_ticket(p.counters + ptg1 * WARPS + warp);
+            if (pend0 && !tk_taken && !skip0) e0 = take_ticket(p.counters + ptg0 * WARPS + warp);
+            if (pend1 && !by_peek) e1 = take_ticket(p.counters + ptg1 * WARPS + warp);
         }
-        t0 = __shfl_sync(0xffffffffu, t0, 0);
-        t1 = __shfl_sync(0xffffffffu, t1, 0);
-        __syncwarp();   // every lane's loads below are ordered after lane 0's acquire
-        const bool use[2] = {pend0 && t0 == static_cast<uint32_t>(info_last(pinfo0) - info_first(pinfo0)),
-                             pend1 && t1 == static_cast<uint32_t>(info_last(pinfo1) - info_first(pinfo1))};
+        e0 = __shfl_sync(0xffffffffu, e0, 0);
+        e1 = __shfl_sync(0xffffffffu, e1, 0);
+        const uint32_t t0 = __shfl_sync(0xffffffffu, tk0, 0);
+        const uint32_t need0 = static_cast<uint32_t>(info_last(pinfo0) - info_first(pinfo0));
+        const uint32_t need1 = static_cast<uint32_t>(info_last(pinfo1) - info_first(pinfo1));
+        const bool use[2] = {pend0 && (tk_taken ? t0 == need0 : (skip0 || e0 == need0)),
+                             pend1 && (by_peek || e1 == need1)};
         const int tgs[2] = {ptg0, ptg1};
         const uint32_t infos[2] = {pinfo0, pinfo1};
-        if (use[0] || use[1]) reduce_split_tiles<C>(p, use, tgs, infos, warp, lane, out);
+        if (use[0] || use[1]) {
+            fence_acq_rel_gpu();   // acquire: the other contributors' partial sums are visible
+            __syncwarp();
+            reduce_split_tiles<C>(p, use, tgs, infos, warp, lane, out);
+        }
     }
 }
 
