@@ -424,14 +424,13 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     // Split segments (at most two per CTA: its first and its last) publish
     // their partial sums at once.  Indexed by partial slot.
     //  * A split segment that ends before the CTA's last unit takes its ticket
-    //    at the next phase end, just before the barrier, when this warp has no
-    //    loads in flight (the release fence is cheap there); the count is read
-    //    after the loop.
+    //    at the next phase end, just before the barrier (the count is read
+    //    after the loop).
     //  * The segment that runs to the CTA's last unit reads its tile's counter
-    //    when it starts.  If every other contributor had already taken its
-    //    ticket, this CTA is the last one by construction: it takes no ticket
-    //    and goes straight to the reduction after the loop.  Otherwise it takes
-    //    its ticket after the loop.
+    //    when that unit starts.  If every other contributor had already taken
+    //    its ticket, this CTA is the last one by construction: it takes no
+    //    ticket and goes straight to the reduction after the loop.  Otherwise
+    //    it takes its ticket after the loop.
     bool pend0 = false, pend1 = false;
     int ptg0 = 0, ptg1 = 0;
     uint32_t pinfo0 = 0, pinfo1 = 0;
@@ -458,11 +457,10 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         }
 
         if (seg_start && rel > 0) begin_segment(true);
-        if (C::ET && seg_start && live) {
-            const bool to_end = rel + (p.nblocks - b) >= nunits;           // runs to the CTA's last unit
-            const bool whole = b == 0 && rel + p.nblocks <= nunits;        // owns the tile-group outright
-            if (to_end && !whole && lane == 0) peek = load_relaxed(p.counters + tile);
-        }
+        // the last unit of a split segment: read its tile's counter (the other
+        // contributors have had the whole kernel to take their tickets)
+        if (C::ET && rel + 1 == nunits && live && !(b_first == 0 && b + 1 == p.nblocks) && lane == 0)
+            peek = load_relaxed(p.counters + tile);
 
         if (live) {
             // the block after next: pull it toward L2 now, so the register
