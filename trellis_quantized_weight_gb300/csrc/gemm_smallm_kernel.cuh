@@ -463,14 +463,6 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             peek = load_relaxed(p.counters + tile);
 
         if (live) {
-            // the block after next: pull it toward L2 now, so the register
-            // prefetch issued one unit ahead finds it there
-            if (b + 2 < p.nblocks && rel + 2 < nunits) {
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    if (ok[r] && lg == 0)
-                        asm volatile("prefetch.global.L2 [%0];" :: "l"(rp[r] + (b + 2) * (kGroupsPerBlock * KB)));
-            }
             uint32_t nw[R][KB];
             if (!seg_end) {
                 load_block_group<KB, R>(rp, ok, b + 1, lg, nw);
