@@ -27,9 +27,9 @@
  * float(w)*float(x) in fp32 and rounds each output once to bf16 (nearest even).
  *
  * Accepted geometry: k in {2, 3, 4}, L == 12, T == 256, K a positive multiple
- * of T, N >= 1, and for trellis_gemm 1 <= M <= 16 (CUDA cores) or M == 64
- * (tensor cores).  Anything else returns TRELLIS_ERR_UNSUPPORTED or
- * TRELLIS_ERR_SHAPE before any launch.
+ * of T, N >= 1, and for trellis_gemm 1 <= M <= 65536 (M <= 16 on the CUDA
+ * cores, larger M on the tensor cores).  Anything else returns
+ * TRELLIS_ERR_UNSUPPORTED or TRELLIS_ERR_SHAPE before any launch.
  *
  * Every call is asynchronous on `stream` (0 = the legacy default stream): it
  * validates its arguments on the host, enqueues its kernels and returns
@@ -102,11 +102,14 @@ int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, 
  *   codes   device, uint32 [N, K*k/32], 16-byte aligned.
  *   scales  device, bf16 [N].
  *   out     device, bf16 [M, N]; fully overwritten.
- *   1 <= M <= 16, or M == 64.
+ *   1 <= M <= 65536.
  *
- * For M == 64 the decoded bf16 weight tiles are multiplied on the tensor
- * cores (tcgen05, fp32 accumulation in tensor memory); that path needs no
- * workspace and its waits are bounded (see trellis_device_status).
+ * For M > 16 the decoded bf16 weight tiles are multiplied on the tensor cores
+ * (tcgen05, fp32 accumulation in tensor memory), in chunks of 64 activation
+ * rows (one launch per chunk; each chunk decodes the weights again; for M > 64
+ * not a multiple of 64 the last chunk overlaps the one before and rewrites
+ * those rows with the same bits); that path needs no workspace and its waits
+ * are bounded (see trellis_device_status).
  *
  * The summation order is fixed by the launch geometry, so repeated calls on
  * the same device give identical bits.  The kernel balances work across all
@@ -116,8 +119,7 @@ int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, 
  * later calls reuse it, so that first call must not happen during stream
  * capture, and calls that use it must not overlap on the GPU (use
  * trellis_gemm_ws with separate workspaces for concurrent streams).
- * Errors: as trellis_decode, plus M outside 1..16 and not 64 ->
- * TRELLIS_ERR_UNSUPPORTED.
+ * Errors: as trellis_decode, plus M outside 1..65536 -> TRELLIS_ERR_UNSUPPORTED.
  */
 int trellis_gemm(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M, int K,
                  int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);

@@ -104,6 +104,46 @@ def test_gemm_m64_tensor_cores(tq, oracle_lib, k, N, K):
     assert_gemm_close(got, ref, refabs, f"M=64 N={N} K={K} k={k}")
 
 
+@pytest.mark.parametrize("M", [17, 33, 63, 65, 100, 128, 200])
+@pytest.mark.parametrize("k", [2, 4])
+def test_gemm_general_m_tensor_cores(tq, oracle_lib, M, k):
+    """M > 16 runs on tcgen05 in chunks of 64 activation rows; a partial chunk's
+    missing rows are zero-filled by the TMA and never stored: the rows after
+    the output (sentinel-filled) stay untouched."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    N, K = 300, 512
+    x, codes, scales = _inputs(M, K, N, k, seed=1700 + 3 * M + k)
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    pad = 8
+    out = torch.full(((M + pad) * N,), 0x7FC1, dtype=torch.int16, device="cuda")
+    rc = binding.abi_gemm(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256,
+                          out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, binding.status_string(rc)
+    torch.cuda.synchronize()
+    assert binding.load().trellis_device_status(None) == 0
+    bits = out.cpu().numpy().view(np.uint16)
+    got = bits[: M * N].reshape(M, N)
+    assert np.all(bits[M * N:] == 0x7FC1), "rows beyond M were written"
+    w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+    ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+    assert_gemm_close(got, ref, refabs, f"M={M} N={N} K={K} k={k}")
+
+
+def test_gemm_m100_one_hot_is_exact(tq, oracle_lib):
+    """Across two 64-row chunks each row of x selects a weight column, bit for bit."""
+    N, K, k, M = 256, 1024, 3, 100
+    _, codes, scales = _inputs(1, K, N, k, seed=642)
+    w = oracle_lib.decode(codes, scales, K, N, k)
+    cols = [(53 * i + 11) % K for i in range(M)]
+    e = np.zeros((M, K), np.uint16)
+    for i, j in enumerate(cols):
+        e[i, j] = 0x3F80
+    got = host_bits(tq.gemm(dev_bf16(e), dev_codes(codes), dev_bf16(scales), k))
+    for i, j in enumerate(cols):
+        assert np.array_equal(got[i], w[:, j]), i
+
+
 def test_gemm_m64_one_hot_is_exact(tq, oracle_lib):
     """Each of the 64 rows of x selects a different weight column, bit for bit."""
     N, K, k = 256, 1024, 4

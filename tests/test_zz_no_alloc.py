@@ -16,7 +16,8 @@ import pytest
 
 pytestmark = pytest.mark.gpu
 
-FAKE = 0x10000   # aligned, never dereferenced: only used where validation rejects first
+FAKE = 0x10000   # aligned, never dereferenced: only in calls that validation rejects before any
+                 # launch (a call that could pass validation must use real device buffers)
 
 
 @pytest.fixture(scope="module")
@@ -73,7 +74,9 @@ def test_noalloc_matches_gemm_ws(lib, M, K, N, k):
 def test_noalloc_rejects_bad_arguments(lib):
     assert lib.trellis_gemm_noalloc(0, FAKE, FAKE, 8, 5120, 64, 3, 12, 256, FAKE, None) == -1
     assert lib.trellis_gemm_noalloc(FAKE + 2, FAKE, FAKE, 8, 5120, 64, 3, 12, 256, FAKE, None) == -4
-    assert lib.trellis_gemm_noalloc(FAKE, FAKE, FAKE, 17, 5120, 64, 3, 12, 256, FAKE, None) == -3
+    # M outside 1..65536 (every M inside it is accepted and would launch)
+    assert lib.trellis_gemm_noalloc(FAKE, FAKE, FAKE, 0, 5120, 64, 3, 12, 256, FAKE, None) == -3
+    assert lib.trellis_gemm_noalloc(FAKE, FAKE, FAKE, 65537, 5120, 64, 3, 12, 256, FAKE, None) == -3
     assert lib.trellis_gemm_noalloc(FAKE, FAKE, FAKE, 8, 5000, 64, 3, 12, 256, FAKE, None) == -2
 
 

@@ -169,7 +169,7 @@ __device__ __forceinline__ void tc_load_group(const uint32_t* __restrict__ row_c
 template <int KB>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
-               uint16_t* __restrict__ out, int K, int N, int row_words,
+               uint16_t* __restrict__ out, int M, int K, int N, int row_words,
                const __grid_constant__ CUtensorMap x_map) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,9 +295,11 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             const int n = n0 + 32 * sub + lane;
             if (n < N) {
+                // activation rows m >= M were zero-filled by the TMA; not stored
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    out[static_cast<size_t>(16 * colq + j) * N + n] = bf16_bits_rn(__uint_as_float(r[j]));
+                    if (16 * colq + j < M)
+                        out[static_cast<size_t>(16 * colq + j) * N + n] = bf16_bits_rn(__uint_as_float(r[j]));
             }
         }
     } else if (warp == kTcTmaWarp) {
@@ -362,13 +364,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// x [64, K] bf16 row-major seen as a 3-D tensor (8 k, m, K/8): a box of
-// (8, 8, 16) is one 8-row group of 16 k-adjacent core matrices, laid out in
-// shared memory exactly as the MMA's K-major no-swizzle operand.
-bool make_x_map(CUtensorMap* map, const uint16_t* x, int K) {
+// x [M, K] bf16 row-major (M <= 64 rows of this chunk) seen as a 3-D tensor
+// (8 k, m, K/8): a box of (8, 8, 16) is one 8-row group of 16 k-adjacent core
+// matrices, laid out in shared memory exactly as the MMA's K-major no-swizzle
+// operand.  Rows m >= M of the 64-row tile lie outside the tensor and are
+// filled with zeros.
+bool make_x_map(CUtensorMap* map, const uint16_t* x, int M, int K) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
-    const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(kTcM), static_cast<cuuint64_t>(K / 8)};
+    const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 8)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 16};
     const cuuint32_t box[3] = {8, 8, kTcStageK / 8};
     const cuuint32_t estr[3] = {1, 1, 1};
@@ -377,11 +381,17 @@ bool make_x_map(CUtensorMap* map, const uint16_t* x, int K) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One launch per chunk of 64 activation rows (each chunk decodes the weights
+// again; the launches are programmatically chained on the stream).  Only
+// M < 64 runs a partial chunk; for larger M the last chunk is moved back to end
+// at row M, so it is full and overlaps the one before: the overlapping rows are
+// computed again with identical bits (each output is its own dot product) and
+// written again after the earlier launch (stream order).  A chunk of very few
+// rows would make most of the TMA box fall outside the tensor, which measured
+// several times slower.
 template <int KB>
-int launch_tc_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K, int N,
+int launch_tc_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
                        uint16_t* out, cudaStream_t stream) {
-    CUtensorMap map;
-    if (!make_x_map(&map, x, K)) return -5;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(gemm_tc_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes) !=
@@ -390,20 +400,28 @@ int launch_tc_instance(const uint16_t* x, const uint32_t* codes, const uint16_t*
         attr_set = true;
     }
     const int grid = (N + kTcRows - 1) / kTcRows;
-    const cudaError_t e = launch_programmatic(gemm_tc_kernel<KB>, static_cast<unsigned>(grid),
-                                              static_cast<unsigned>(kTcThreads), kTcSmemBytes, stream,
-                                              codes, scales, out, K, N, K / 32 * KB, map);
-    return e == cudaSuccess ? 0 : -5;
+    for (int m = 0; m < M; m += kTcM) {
+        const int m0 = (M > kTcM && m + kTcM > M) ? M - kTcM : m;
+        const int mc = (M - m0) < kTcM ? (M - m0) : kTcM;
+        CUtensorMap map;
+        if (!make_x_map(&map, x + static_cast<size_t>(m0) * K, mc, K)) return -5;
+        const cudaError_t e = launch_programmatic(gemm_tc_kernel<KB>, static_cast<unsigned>(grid),
+                                                  static_cast<unsigned>(kTcThreads), kTcSmemBytes, stream,
+                                                  codes, scales, out + static_cast<size_t>(m0) * N, mc, K, N,
+                                                  K / 32 * KB, map);
+        if (e != cudaSuccess) return -5;
+    }
+    return 0;
 }
 
 }  // namespace
 
-int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
+int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N, int k,
                    uint16_t* out, cudaStream_t stream) {
     switch (k) {
-        case 2: return launch_tc_instance<2>(x, codes, scales, K, N, out, stream);
-        case 3: return launch_tc_instance<3>(x, codes, scales, K, N, out, stream);
-        case 4: return launch_tc_instance<4>(x, codes, scales, K, N, out, stream);
+        case 2: return launch_tc_instance<2>(x, codes, scales, M, K, N, out, stream);
+        case 3: return launch_tc_instance<3>(x, codes, scales, M, K, N, out, stream);
+        case 4: return launch_tc_instance<4>(x, codes, scales, M, K, N, out, stream);
         default: return -3;
     }
 }

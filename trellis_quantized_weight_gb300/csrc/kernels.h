@@ -50,8 +50,9 @@ int launch_gemm_smallm(const uint16_t* x, const uint32_t* codes, const uint16_t*
                        int K, int N, int k, uint16_t* out, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream, const DeviceInfo& dev);
 
-// Fused decode-and-multiply for M == 64 on the tensor cores (tcgen05).
-int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
+// Fused decode-and-multiply for M > 16 on the tensor cores (tcgen05), in
+// chunks of 64 activation rows.
+int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N, int k,
                    uint16_t* out, cudaStream_t stream);
 // Reads and clears the tensor-core kernel's device error word (bit 0: a
 // bounded wait gave up).  Returns 0 or a trellis_status.

@@ -49,9 +49,11 @@ int check_geometry(int K, int N, int k, int L, int T) {
     return TRELLIS_OK;
 }
 
-// 1 <= M <= 16 runs on the CUDA cores; M == 64 on the tensor cores.
-constexpr int kTensorCoreM = 64;
-bool gemm_m_supported(int M) { return (M >= 1 && M <= 16) || M == kTensorCoreM; }
+// 1 <= M <= 16 runs on the CUDA cores; 16 < M <= kMaxM on the tensor cores.
+constexpr int kSmallMMax = 16;
+constexpr int kMaxM = 65536;
+bool gemm_m_supported(int M) { return M >= 1 && M <= kMaxM; }
+bool gemm_on_tensor_cores(int M) { return M > kSmallMMax; }
 
 int check_codes(const uint32_t* codes, const uint16_t* scales) {
     if (codes == nullptr || scales == nullptr) return TRELLIS_ERR_NULL;
@@ -142,7 +144,7 @@ int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t
     int rc = check_geometry(K, N, k, L, T);
     if (rc != TRELLIS_OK) return rc;
     if (!gemm_m_supported(M)) return TRELLIS_ERR_UNSUPPORTED;
-    if (M == kTensorCoreM) {   // the tensor-core path needs no workspace
+    if (gemm_on_tensor_cores(M)) {   // the tensor-core path needs no workspace
         *bytes = 0;
         return TRELLIS_OK;
     }
@@ -158,7 +160,7 @@ int trellis_gemm_ws(const uint16_t* x, const uint32_t* codes, const uint16_t* sc
                     cudaStream_t stream) {
     int rc = check_gemm(x, codes, scales, M, K, N, k, L, T, out);
     if (rc != TRELLIS_OK) return rc;
-    if (M == kTensorCoreM) return trellis::launch_gemm_tc(x, codes, scales, K, N, k, out, stream);
+    if (gemm_on_tensor_cores(M)) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, out, stream);
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
@@ -174,7 +176,7 @@ int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scale
                  int k, int L, int T, uint16_t* out, cudaStream_t stream) {
     int rc = check_gemm(x, codes, scales, M, K, N, k, L, T, out);
     if (rc != TRELLIS_OK) return rc;
-    if (M == kTensorCoreM) return trellis::launch_gemm_tc(x, codes, scales, K, N, k, out, stream);
+    if (gemm_on_tensor_cores(M)) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, out, stream);
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
