@@ -46,6 +46,7 @@ if ROOT not in sys.path:
 HEADLINE = "gemm_m8_k5120_n17408_k3"
 METRIC = "trellis GEMM packed-weight GB/s"
 METRIC_DECODE = "trellis decode packed-weight GB/s"
+METRIC_GATEUP = "trellis gate/up GEMM packed-weight GB/s"
 DECODE_OPS_PER_WEIGHT = 10        # algorithmic integer/fp32 ops per decoded weight
 ALU_LANES_PER_SM = 128            # 4 sub-partitions x 32 lanes, one op per lane per clock
 
@@ -238,7 +239,26 @@ def run_ours(args, wl):
     dcodes = [to_dev(codes, torch, "u32") for _ in range(n_rot)]
     stream = torch.cuda.Stream()
     s_handle = stream.cuda_stream
-    if args.entry == "gemm":
+    n_mats = 2 if args.entry == "gateup" else 1
+    if args.entry == "gateup":
+        # the up projection: a second matrix of the same shape, its own seed
+        from trellis_quantized_weight_gb300 import synth
+        _, codes_u, scales_u = synth.small(wl.M, wl.K, wl.N, wl.k, seed=wl.seed + 0x1000,
+                                           sigma=wl.sigma).generate()
+        dcodes_u = [to_dev(codes_u, torch, "u32") for _ in range(n_rot)]
+        dscales_u = to_dev(scales_u, torch, "bf16")
+        outs = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+        ws_bytes = binding.gemm_gateup_workspace_bytes(wl.M, wl.K, wl.N, wl.k)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+
+        def call(i):
+            rc = lib.trellis_gemm_gateup(dx.data_ptr(), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
+                                         dcodes_u[i % n_rot].data_ptr(), dscales_u.data_ptr(), wl.M, wl.K,
+                                         wl.N, wl.k, wl.L, wl.T, outs[0].data_ptr(), outs[1].data_ptr(),
+                                         outs[2].data_ptr(), ws.data_ptr(), ws.numel(), s_handle)
+            if rc != 0:
+                raise RuntimeError(f"trellis_gemm_gateup failed: {binding.status_string(rc)}")
+    elif args.entry == "gemm":
         out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
         ws_bytes = binding.gemm_workspace_bytes(wl.M, wl.K, wl.N, wl.k)
         ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
@@ -319,6 +339,12 @@ def run_ours(args, wl):
         if args.entry == "decode":
             from trellis_quantized_weight_gb300 import decode as tq_decode
             hout = torch.empty((wl.N, wl.K), dtype=torch.bfloat16).pin_memory()
+        if args.entry == "gateup":
+            from trellis_quantized_weight_gb300 import gemm_gateup as tq_gateup
+            hcu = torch.from_numpy(codes_u.view(np.int32)).pin_memory()
+            hsu = torch.from_numpy(scales_u.view(np.int16)).view(torch.bfloat16).pin_memory()
+            dcu2 = torch.empty_like(dcodes_u[0])
+            dsu2 = torch.empty_like(dscales_u)
 
         def e2e_step():
             dc2.copy_(hc, non_blocking=True)
@@ -326,6 +352,11 @@ def run_ours(args, wl):
             if args.entry == "gemm":
                 dx2.copy_(hx, non_blocking=True)
                 y = tq_gemm(dx2, dc2, ds2, wl.k)
+            elif args.entry == "gateup":
+                dx2.copy_(hx, non_blocking=True)
+                dcu2.copy_(hcu, non_blocking=True)
+                dsu2.copy_(hsu, non_blocking=True)
+                y = tq_gateup(dx2, dc2, ds2, dcu2, dsu2, wl.k)[2]   # the activation
             else:
                 y = tq_decode(dc2, ds2, wl.K, wl.k)
             hout.copy_(y, non_blocking=True)
@@ -346,8 +377,8 @@ def run_ours(args, wl):
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / n_e2e
         (e2e_ms,) = max_over_ranks([e2e_ms], device="cuda")
-        h2d = (hx.numel() * 2 if args.entry == "gemm" else 0) + hc.numel() * 4 + hs.numel() * 2
-        e2e = {"value": round(whole_job_gbs(world, wl.code_bytes, e2e_ms), 2), "unit": "GB/s",
+        h2d = (hx.numel() * 2 if args.entry != "decode" else 0) + n_mats * (hc.numel() * 4 + hs.numel() * 2)
+        e2e = {"value": round(whole_job_gbs(world, n_mats * wl.code_bytes, e2e_ms), 2), "unit": "GB/s",
                "us_per_call": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": hout.numel() * 2}
 
@@ -359,16 +390,20 @@ def run_ours(args, wl):
     t_kernel = kernel_ms * 1e-3
     flops = 0
     tensor_peak = float(peaks.get("bf16_tflops") or 1900.0)
-    if args.entry == "gemm" and wl.M == 64:
+    if args.entry in ("gemm", "gateup") and wl.M > 16:
         # tensor-core path: the decode runs on the ALUs, the M FMAs per weight
         # are a dense bf16 contraction on the tensor cores
-        ops = wl.weights * DECODE_OPS_PER_WEIGHT
-        flops = 2 * wl.M * wl.N * wl.K
-        hbm_bytes = wl.code_bytes + wl.M * wl.K * 2 + wl.M * wl.N * 2
+        ops = n_mats * wl.weights * DECODE_OPS_PER_WEIGHT
+        flops = n_mats * 2 * wl.M * wl.N * wl.K
+        hbm_bytes = n_mats * (wl.code_bytes + wl.M * wl.N * 2) + wl.M * wl.K * 2
         kernel_name = "gemm_tc"
-    elif args.entry == "gemm":
-        ops = wl.weights * (DECODE_OPS_PER_WEIGHT + wl.M)
-        hbm_bytes = wl.code_bytes + wl.M * wl.K * 2 + wl.M * wl.N * 2
+    elif args.entry in ("gemm", "gateup"):
+        # gate/up: both matrices in one launch, plus the elementwise activation
+        # (read 2 and write 1 bf16 [M, N]; bytes counted, no ALU ops)
+        ops = n_mats * wl.weights * (DECODE_OPS_PER_WEIGHT + wl.M)
+        hbm_bytes = n_mats * (wl.code_bytes + wl.M * wl.N * 2) + wl.M * wl.K * 2
+        if args.entry == "gateup":
+            hbm_bytes += 3 * wl.M * wl.N * 2
         kernel_name = "gemm_smallm"
     else:
         ops = wl.weights * DECODE_OPS_PER_WEIGHT
@@ -408,9 +443,16 @@ def run_ours(args, wl):
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} rows x K={wl.K} of {wl.name} (decode + product), {dt:.1f} s wall"}
 
-    value = whole_job_gbs(world, wl.code_bytes, ms_step)
+    value = whole_job_gbs(world, n_mats * wl.code_bytes, ms_step)
+    # our kernels per step: one per 64-row chunk per matrix on the tensor cores,
+    # else one small-M launch; plus the gate/up activation
+    chunks = (wl.M + 63) // 64 if wl.M > 16 and args.entry != "decode" else 1
+    launches_per_step = n_mats * chunks if wl.M > 16 and args.entry != "decode" else 1
+    if args.entry == "gateup":
+        launches_per_step += 1
     line = {
-        "metric": METRIC if args.entry == "gemm" else METRIC_DECODE, "value": round(value, 2), "unit": "GB/s",
+        "metric": {"gemm": METRIC, "decode": METRIC_DECODE, "gateup": METRIC_GATEUP}[args.entry],
+        "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "us_per_call": round(ms_step * 1e3, 2), "isolated_call_us": round(isolated_ms * 1e3, 2),
@@ -419,7 +461,7 @@ def run_ours(args, wl):
         "config": {"workload": wl.name, "entry": "trellis_" + args.entry, "M": wl.M, "K": wl.K, "N": wl.N,
                    "k": wl.k, "L": wl.L, "T": wl.T, "parallelism": f"replicas{world}",
                    "l2": f"rotating {n_rot} code copies ({n_rot * wl.code_bytes / 1e6:.0f} MB > 2x L2)"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks, "host_wall_s": round(t_host, 3),
     }
     if rank == 0:
@@ -486,8 +528,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
-    ap.add_argument("--entry", choices=["gemm", "decode"], default="gemm",
-                    help="time the fused product (default) or the dense decode")
+    ap.add_argument("--entry", choices=["gemm", "decode", "gateup"], default="gemm",
+                    help="time the fused product (default), the dense decode, or the gate/up pair with its activation")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)

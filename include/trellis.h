@@ -163,6 +163,38 @@ int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *sc
 int trellis_device_status(cudaStream_t stream);
 
 /*
+ * trellis_gemm_gateup — the two projections of a gated MLP that share x, in
+ * one pass over x: out_gate = x * W_gate^T and out_up = x * W_up^T (each as
+ * trellis_gemm computes it, the same bits as two trellis_gemm calls up to the
+ * split-K summation order), and, when out_act is not NULL,
+ * out_act = bf16(silu(out_gate) * out_up) elementwise with
+ * silu(v) = v / (1 + e^-v) evaluated in fp32 from the bf16 outputs.  The
+ * fused gate/up kernels are named on the page "mlx-bun 0.4.0 -> 0.5.0" without
+ * their bodies; this is the plainest reading (two trellis products sharing x,
+ * an optional SiLU-gated product).
+ *
+ *   codes_gate/scales_gate, codes_up/scales_up: two weight matrices [N, K], as
+ *           for trellis_gemm (same k, K, N).
+ *   out_gate, out_up: device, bf16 [M, N]; out_act: bf16 [M, N] or NULL.
+ *   workspace: as trellis_gemm_ws, sized by trellis_gemm_gateup_workspace_size
+ *           (0 bytes for M > 16).
+ * For M <= 16 both matrices' rows are decoded in one launch (the activations
+ * are staged once); for M > 16 each matrix takes the tensor-core path.
+ * Errors: as trellis_gemm_ws for either matrix; out_act misaligned ->
+ * TRELLIS_ERR_ALIGN.
+ */
+int trellis_gemm_gateup(const uint16_t *x, const uint32_t *codes_gate, const uint16_t *scales_gate,
+                        const uint32_t *codes_up, const uint16_t *scales_up, int M, int K, int N, int k,
+                        int L, int T, uint16_t *out_gate, uint16_t *out_up, uint16_t *out_act,
+                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * trellis_gemm_gateup_workspace_size — bytes of workspace trellis_gemm_gateup
+ * needs on the current device.  Same validation as trellis_gemm.
+ */
+int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T, size_t *bytes);
+
+/*
  * trellis_gemm_noalloc — trellis_gemm for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a library convenience.
  *

@@ -74,6 +74,8 @@ class Oracle:
         lib.oracle_decode_rows.restype = ctypes.c_int
         lib.oracle_decode_rows.argtypes = [u32p, u16p, i64, i64, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, i64, i64, u16p]
+        lib.oracle_silu_mul.restype = None
+        lib.oracle_silu_mul.argtypes = [u16p, u16p, i64, u16p]
         lib.oracle_gemm_dense.restype = ctypes.c_int
         lib.oracle_gemm_dense.argtypes = [u16p, u16p, i64, i64, i64,
                                           ctypes.POINTER(ctypes.c_float),
@@ -136,6 +138,17 @@ class Oracle:
         """Decode rows [n0, n1) then multiply: (ref [M, n1-n0], refabs [M, n1-n0])."""
         w = self.decode(codes, scales_bf16, K, N, k, L, T, rows)
         return self.gemm_dense(x_bf16, w)
+
+    def silu_mul(self, g_bf16: np.ndarray, u_bf16: np.ndarray) -> np.ndarray:
+        """act = bf16(silu(g) * u) elementwise on bf16 bit arrays of one shape."""
+        g = np.ascontiguousarray(g_bf16, dtype=np.uint16)
+        u = np.ascontiguousarray(u_bf16, dtype=np.uint16)
+        if g.shape != u.shape:
+            raise ValueError("g and u must have one shape")
+        act = np.empty_like(g)
+        self.lib.oracle_silu_mul(_ptr(g, ctypes.c_uint16), _ptr(u, ctypes.c_uint16), g.size,
+                                 _ptr(act, ctypes.c_uint16))
+        return act
 
 
 def _ptr(a: np.ndarray, ctype):

@@ -139,3 +139,18 @@ int oracle_gemm_dense(const uint16_t *x, const uint16_t *W, int64_t M, int64_t K
     }
     return 0;
 }
+
+/* ---- gate/up: act = bf16(silu(g) * u) --------------------------------------- */
+/* The SiLU-gated product of two projections that share x.  The page
+ * "mlx-bun 0.4.0 -> 0.5.0" (package/src/model/trellis-linear.ts) imports fused
+ * gate/up kernels without showing their bodies; reading taken: silu(v) =
+ * v / (1 + e^-v) of the bf16 gate output times the bf16 up output, evaluated
+ * exactly (double) and rounded to fp32, then to bf16 (nearest even). */
+void oracle_silu_mul(const uint16_t *g, const uint16_t *u, int64_t n, uint16_t *act) {
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = (double)oracle_bf16_to_f32(g[i]);
+        const double s = v / (1.0 + exp(-v));
+        act[i] = oracle_f32_to_bf16((float)(s * (double)oracle_bf16_to_f32(u[i])));
+    }
+}
+

@@ -14,5 +14,6 @@ int oracle_decode_rows(const uint32_t *codes, const uint16_t *scales, int64_t K,
                        int k, int L, int T, int64_t n0, int64_t n1, uint16_t *out);
 int oracle_gemm_dense(const uint16_t *x, const uint16_t *W, int64_t M, int64_t K, int64_t nrows,
                       float *ref, double *refabs);
+void oracle_silu_mul(const uint16_t *g, const uint16_t *u, int64_t n, uint16_t *act);
 
 #endif

@@ -31,6 +31,12 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32)
 
 
+def ulp_bf16_of(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (the smallest normal spacing below 2^-126)."""
+    a = np.maximum(np.abs(np.asarray(v, dtype=np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
 def _threads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 

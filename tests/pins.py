@@ -256,6 +256,28 @@ def pin_gemm(o, seed=11):
     assert np.all(np.abs((a.astype(np.float64) + b) - c) <= 1e-6 * (cab + 1e-30) + 1e-30)
 
 
-ALL_PINS = [pin_golden_worked_examples, pin_window_bruteforce, pin_hash_exhaustive,
+def pin_silu_mul(o, seed=21):
+    """Gate/up activation act = bf16(silu(g) * u), silu(v) = v / (1 + e^-v).
+    Values worked out by hand from that definition: silu(1) = 0.731058...
+    -> bf16 0x3F3B (0.73046875); silu(2) = 1.761594... -> 0x3FE1 (1.7578125);
+    silu(64) = 64 - 64 e^-64 -> 0x4280 (64.0); silu(0) = 0; with u = 2 the
+    product doubles exactly (0x3FBB = 1.4609375).  Also: doubling u doubles
+    every result exactly (power-of-two scaling commutes with each rounding)."""
+    g = np.array([0x0000, 0x3F80, 0x4000, 0x4280, 0x3F80], np.uint16)
+    u = np.array([0x3F80, 0x3F80, 0x3F80, 0x3F80, 0x4000], np.uint16)
+    want = np.array([0x0000, 0x3F3B, 0x3FE1, 0x4280, 0x3FBB], np.uint16)
+    got = o.silu_mul(g, u)
+    assert np.array_equal(got, want), (got, want)
+    rng = np.random.default_rng(seed)
+    gf = rng.normal(0.0, 2.0, 4096).astype(np.float32)
+    uf = rng.normal(0.0, 1.0, 4096).astype(np.float32)
+    gb, ub = bf16_bits_torch(gf), bf16_bits_torch(uf)
+    ub2 = bf16_bits_torch(2.0 * bf16_to_f32(ub))
+    a1 = bf16_to_f32(o.silu_mul(gb, ub))
+    a2 = bf16_to_f32(o.silu_mul(gb, ub2))
+    assert np.array_equal(a2, 2.0 * a1)
+
+
+ALL_PINS = [pin_silu_mul, pin_golden_worked_examples, pin_window_bruteforce, pin_hash_exhaustive,
             pin_value_exhaustive, pin_bf16_rounding, pin_decode_composition,
             pin_scale_linearity, pin_gemm]

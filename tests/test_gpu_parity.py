@@ -144,6 +144,59 @@ def test_gemm_m100_one_hot_is_exact(tq, oracle_lib):
         assert np.array_equal(got[i], w[:, j]), i
 
 
+@pytest.mark.parametrize("M", [1, 5, 8, 15, 16, 17, 64, 100])
+@pytest.mark.parametrize("k", [2, 4])
+def test_gemm_gateup(tq, oracle_lib, M, k):
+    """Gate and up projections sharing x in one call: each output against the
+    oracle product, act = bf16(silu(gate) * up) against the oracle's activation
+    of the GPU's own gate/up outputs (within 1 bf16 ulp: fp32 exp on the GPU),
+    and nothing written past either [M, N] output (sentinel rows)."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    from helpers import ulp_bf16_of
+    N, K = 300, 1024
+    x, cg, sg = _inputs(M, K, N, k, seed=2100 + 5 * M + k)
+    _, cu, su = _inputs(M, K, N, k, seed=2200 + 5 * M + k)
+    dx, dcg, dsg, dcu, dsu = dev_bf16(x), dev_codes(cg), dev_bf16(sg), dev_codes(cu), dev_bf16(su)
+    pad = 4
+    bufs = [torch.full(((M + pad) * N,), 0x7FC1, dtype=torch.int16, device="cuda") for _ in range(3)]
+    need = binding.gemm_gateup_workspace_bytes(M, K, N, k)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+    rc = binding.load().trellis_gemm_gateup(dx.data_ptr(), dcg.data_ptr(), dsg.data_ptr(), dcu.data_ptr(),
+                                            dsu.data_ptr(), M, K, N, k, 12, 256, bufs[0].data_ptr(),
+                                            bufs[1].data_ptr(), bufs[2].data_ptr(), ws.data_ptr(), ws.numel(),
+                                            torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, binding.status_string(rc)
+    torch.cuda.synchronize()
+    assert binding.load().trellis_device_status(None) == 0
+    host = [b.cpu().numpy().view(np.uint16) for b in bufs]
+    for h in host:
+        assert np.all(h[M * N:] == 0x7FC1), "rows beyond M were written"
+    g, u, a = (h[: M * N].reshape(M, N) for h in host)
+    for got, codes, scales, what in ((g, cg, sg, "gate"), (u, cu, su, "up")):
+        w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+        ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+        assert_gemm_close(got, ref, refabs, f"{what} M={M} k={k}")
+    ref_act = bf16_to_f32(oracle_lib.silu_mul(g, u)).astype(np.float64)
+    err = np.abs(bf16_to_f32(a).astype(np.float64) - ref_act)
+    assert np.all(err <= ulp_bf16_of(ref_act)), f"act: max excess {float((err - ulp_bf16_of(ref_act)).max())}"
+
+
+def test_gemm_gateup_without_activation(tq, oracle_lib):
+    """act=False returns no third output; gate and up, over a K long enough to be
+    split across CTAs, match the oracle products."""
+    M, K, N, k = 8, 5120, 2000, 3
+    x, cg, sg = _inputs(M, K, N, k, seed=2301)
+    _, cu, su = _inputs(M, K, N, k, seed=2302)
+    g, u, a = tq.gemm_gateup(dev_bf16(x), dev_codes(cg), dev_bf16(sg), dev_codes(cu), dev_bf16(su), k,
+                             act=False)
+    assert a is None
+    for got, codes, scales, what in ((g, cg, sg, "gate"), (u, cu, su, "up")):
+        w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+        ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+        assert_gemm_close(host_bits(got), ref, refabs, what)
+
+
 def test_gemm_m64_one_hot_is_exact(tq, oracle_lib):
     """Each of the 64 rows of x selects a different weight column, bit for bit."""
     N, K, k = 256, 1024, 4

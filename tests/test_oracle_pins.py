@@ -59,6 +59,10 @@ MUTATIONS = {
     "scale_row0": ("oracle_weight(blk, t, k, L, T, scales[n])", "oracle_weight(blk, t, k, L, T, scales[0])"),
     "gemm_x_row0": ("(double)oracle_bf16_to_f32(x[m * K + kk])", "(double)oracle_bf16_to_f32(x[kk])"),
     "gemm_transposed_w": ("oracle_bf16_to_f32(W[i * K + kk])", "oracle_bf16_to_f32(W[kk * nrows + i])"),
+    "silu_is_sigmoid": ("const double s = v / (1.0 + exp(-v));", "const double s = 1.0 / (1.0 + exp(-v));"),
+    "silu_sign": ("const double s = v / (1.0 + exp(-v));", "const double s = v / (1.0 + exp(v));"),
+    "silu_gate_up_swapped": ("const double v = (double)oracle_bf16_to_f32(g[i]);",
+                             "const double v = (double)oracle_bf16_to_f32(u[i]);"),
 }
 
 

@@ -34,6 +34,8 @@ SIGNATURES = {
     "trellis_gemm_ws": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "trellis_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "trellis_device_status": (_I, [_P]),
+    "trellis_gemm_gateup": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "trellis_gemm_gateup_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
 }
 
 
@@ -96,6 +98,13 @@ def gemm_workspace_bytes(M, K, N, k, L=12, T=256) -> int:
     n = ctypes.c_size_t(0)
     _check(load().trellis_gemm_workspace_size(M, K, N, k, L, T, ctypes.byref(n)),
            "trellis_gemm_workspace_size")
+    return int(n.value)
+
+
+def gemm_gateup_workspace_bytes(M, K, N, k, L=12, T=256) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().trellis_gemm_gateup_workspace_size(M, K, N, k, L, T, ctypes.byref(n)),
+           "trellis_gemm_gateup_workspace_size")
     return int(n.value)
 
 
@@ -177,3 +186,32 @@ def gemm(x, codes, scales, k: int, L: int = 12, T: int = 256, out=None, stream=N
                      out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(x.device, stream))
     _check(rc, "trellis_gemm_ws")
     return out
+
+
+def gemm_gateup(x, codes_gate, scales_gate, codes_up, scales_up, k: int, act: bool = True, L: int = 12,
+                T: int = 256, stream=None):
+    """The two projections that share x: returns (gate [M, N], up [M, N], act [M, N] or None)
+    with act = bf16(silu(gate) * up)."""
+    torch = _torch()
+    _require(x, "x", (torch.bfloat16,), 2)
+    for name, c, sc in (("gate", codes_gate, scales_gate), ("up", codes_up, scales_up)):
+        _require(c, f"codes_{name}", (torch.int32, torch.uint32), 2)
+        _require(sc, f"scales_{name}", (torch.bfloat16,), 1)
+    M, K = x.shape
+    N = codes_gate.shape[0]
+    if tuple(codes_up.shape) != tuple(codes_gate.shape) or codes_gate.shape[1] * 32 != K * k:
+        raise ValueError("codes_gate and codes_up must both be [N, K*k/32]")
+    if scales_gate.numel() != N or scales_up.numel() != N:
+        raise ValueError("scales must be [N]")
+    g = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    u = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    a = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if act else None
+    nbytes = gemm_gateup_workspace_bytes(M, K, N, k, L, T)
+    ws = _workspace(x.device, max(nbytes, 256))
+    rc = load().trellis_gemm_gateup(x.data_ptr(), codes_gate.data_ptr(), scales_gate.data_ptr(),
+                                    codes_up.data_ptr(), scales_up.data_ptr(), M, K, N, k, L, T,
+                                    g.data_ptr(), u.data_ptr(), a.data_ptr() if act else None,
+                                    ws.data_ptr(), ws.numel(), _stream_handle(x.device, stream))
+    _check(rc, "trellis_gemm_gateup")
+    return g, u, a
+

@@ -6,16 +6,16 @@ namespace trellis {
 
 // 0 when the geometry needs more tile counters than the workspace layout holds.
 template <int MM>
-static size_t ws_bytes_for(int K, int N, int k, const DeviceInfo& dev) {
+static size_t ws_bytes_for(int K, int N, int k, const DeviceInfo& dev, bool two) {
     using C = typename SmallMDefault<MM>::type;
-    const SmallMPlan p = plan_smallm<C>(K, N, k, dev);
+    const SmallMPlan p = plan_smallm<C>(K, N, k, dev, two);
     return smallm_fits_counters<C>(p) ? smallm_workspace_bytes<C>(p) : 0;
 }
 
-size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo& dev) {
+size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo& dev, bool two) {
     switch (M) {
 #define TRELLIS_CASE(MV) \
-    case MV: return ws_bytes_for<MV>(K, N, k, dev);
+    case MV: return ws_bytes_for<MV>(K, N, k, dev, two);
         TRELLIS_CASE(1) TRELLIS_CASE(2) TRELLIS_CASE(3) TRELLIS_CASE(4)
         TRELLIS_CASE(5) TRELLIS_CASE(6) TRELLIS_CASE(7) TRELLIS_CASE(8)
         TRELLIS_CASE(9) TRELLIS_CASE(10) TRELLIS_CASE(11) TRELLIS_CASE(12)
@@ -27,7 +27,15 @@ size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo&
 
 int launch_gemm_smallm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M,
                        int K, int N, int k, uint16_t* out, void* workspace, size_t workspace_bytes,
-                       cudaStream_t stream, const DeviceInfo& dev) {
+                       cudaStream_t stream, const DeviceInfo& dev, const SecondMatrix& second) {
+    if (second.codes != nullptr) {
+        switch (k) {
+            case 2: return launch_smallm2_k<2>(M, x, codes, scales, K, N, out, workspace, workspace_bytes, stream, dev, second);
+            case 3: return launch_smallm2_k<3>(M, x, codes, scales, K, N, out, workspace, workspace_bytes, stream, dev, second);
+            case 4: return launch_smallm2_k<4>(M, x, codes, scales, K, N, out, workspace, workspace_bytes, stream, dev, second);
+            default: return -3;
+        }
+    }
     switch (k) {
         case 2: return launch_smallm_k<2>(M, x, codes, scales, K, N, out, workspace, workspace_bytes, stream, dev);
         case 3: return launch_smallm_k<3>(M, x, codes, scales, K, N, out, workspace, workspace_bytes, stream, dev);

@@ -63,6 +63,13 @@ struct SmallMPlan {
     int base, rem;      // CTA c takes base + (c < rem) units, c*base + min(c, rem) first
     FastDiv div_base1;  // division by base + 1
     FastDiv div_base;   // division by base
+    // Two weight matrices sharing x (gate and up projections): virtual rows
+    // [0, npad) are matrix 0 (the kernel's codes, scales, out), [npad, 2*npad)
+    // matrix 1; npad is N rounded up to whole tile-groups, 0 for one matrix.
+    int npad;
+    const uint32_t* codes2;
+    const uint16_t* scales2;
+    uint16_t* out2;
     float* partials;    // workspace: [P][2][WARPS][R*M*4] fp32
     uint32_t* counters; // workspace: [ntg * WARPS]
 };
@@ -82,7 +89,10 @@ struct SmallMPlan {
 //          range spans a tile-group boundary (each split tile then has two
 //          contributors, one finishing early); the in-loop fence costs more
 //          than it saves otherwise.
-template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1, int UB_ = 2, bool GM_ = false, bool ET_ = false>
+//   TWO    two weight matrices sharing x (gate and up); single-matrix kernels
+//          carry none of the row mapping
+template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1, int UB_ = 2, bool GM_ = false, bool ET_ = false,
+          bool TWO_ = false>
 struct SmallMCfg {
     static constexpr int MM = MM_;
     static constexpr int R = R_;
@@ -101,6 +111,7 @@ struct SmallMCfg {
     static constexpr size_t SMEM_BYTES = TABLE_BYTES + RING * XS_UNIT * sizeof(float);
     static constexpr bool GM = GM_;
     static constexpr bool ET = ET_;
+    static constexpr bool TWO = TWO_;
     static constexpr int GROUP_STRIDE = GM ? 4 : 1;  // lane distance between groups of a slot
 };
 
@@ -114,8 +125,26 @@ struct SmallMDefault {
     static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
     static constexpr bool ET = MM >= 12;
     using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET>;
+    using two = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, true>;   // gate and up
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
+
+// The matrix a tile-group's virtual rows belong to: its codes, scales and
+// output, and the virtual row of its first row.
+struct RowSrc {
+    const uint32_t* codes;
+    const uint16_t* scales;
+    uint16_t* out;
+    int first;
+};
+template <class C>
+__device__ __forceinline__ RowSrc row_source(const SmallMPlan& p, const uint32_t* codes, const uint16_t* scales,
+                                             uint16_t* out, int row0) {
+    if constexpr (C::TWO) {
+        if (row0 >= p.npad) return RowSrc{p.codes2, p.scales2, p.out2, p.npad};
+    }
+    return RowSrc{codes, scales, out, 0};
+}
 
 __device__ __forceinline__ int unit_begin(int c, const SmallMPlan& p) {
     return c * p.base + (c < p.rem ? c : p.rem);
@@ -292,14 +321,15 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
         if (!use[t]) continue;
         const int tile = tgs[t] * WARPS + warp;
         const int row0 = tile * C::ROWS_PER_TILE;
+        const RowSrc rs = row_source<C>(p, nullptr, nullptr, out, row0);
 #pragma unroll
         for (int ep = 0; ep < EP; ++ep) {
             const int e = lane + 32 * ep;
             if (e < E) {
                 const int q = e & 3, rm = e >> 2;
                 const int r = rm / MM, m = rm - r * MM;
-                const int n = row0 + q + 4 * r;
-                if (n < p.N) out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum[t][ep]);
+                const int n = row0 - rs.first + q + 4 * r;
+                if (n < p.N) rs.out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum[t][ep]);
             }
         }
         if (lane == 0) p.counters[tile] = 0u;
@@ -357,19 +387,20 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         seg_info = contributors_info(tg, p);
         tile = tg * WARPS + warp;
         row0 = tile * C::ROWS_PER_TILE;
-        live = row0 < p.N;   // whole tile beyond N: skipped by every CTA alike
+        const RowSrc rs = row_source<C>(p, codes, scales, out, row0);
+        live = row0 - rs.first < p.N;   // whole tile beyond N: skipped by every CTA alike
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int n = row0 + slot + 4 * r;    // this lane's row
-            const int nl = row0 + lslot + 4 * r;  // the row this lane loads codes for
+            const int n = row0 - rs.first + slot + 4 * r;    // this lane's row
+            const int nl = row0 - rs.first + lslot + 4 * r;  // the row this lane loads codes for
             ok[r] = nl < p.N;
             float sr;
             if (prefetched)
                 sr = snext[r];
             else
-                sr = n < p.N ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
+                sr = n < p.N ? bf16_bits_to_f32(__ldg(rs.scales + n)) : 0.0f;
             s2[r] = make_float2(sr, sr);
-            rp[r] = codes + static_cast<size_t>(ok[r] ? nl : 0) * p.row_words;
+            rp[r] = rs.codes + static_cast<size_t>(ok[r] ? nl : 0) * p.row_words;
 #pragma unroll
             for (int m = 0; m < MM; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
         }
@@ -384,13 +415,14 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     // slots 0 .. UB-1).
     if (nunits > 0) {
         const int prow0 = (utg * WARPS + warp) * C::ROWS_PER_TILE;
+        const RowSrc prs = row_source<C>(p, codes, scales, out, prow0);
         if (lg == 0) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const int n = prow0 + lslot + 4 * r;
+                const int n = prow0 - prs.first + lslot + 4 * r;
                 if (n < p.N)
                     asm volatile("prefetch.global.L2 [%0];"
-                                 :: "l"(codes + static_cast<size_t>(n) * p.row_words + b * (kGroupsPerBlock * KB)));
+                                 :: "l"(prs.codes + static_cast<size_t>(n) * p.row_words + b * (kGroupsPerBlock * KB)));
             }
         }
         // x of the first unit: MM rows of 512 bytes, 4 lines each
@@ -470,15 +502,16 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 // the next unit starts tile-group utg + 1 at block 0: request
                 // its codes and scales now
                 const int nrow0 = ((utg + 1) * WARPS + warp) * C::ROWS_PER_TILE;
+                const RowSrc nrs = row_source<C>(p, codes, scales, out, nrow0);
                 bool nok[R];
                 const uint32_t* nrp[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const int n = nrow0 + slot + 4 * r;
-                    const int nl = nrow0 + lslot + 4 * r;
+                    const int n = nrow0 - nrs.first + slot + 4 * r;
+                    const int nl = nrow0 - nrs.first + lslot + 4 * r;
                     nok[r] = nl < p.N;
-                    nrp[r] = codes + static_cast<size_t>(nok[r] ? nl : 0) * p.row_words;
-                    snext[r] = n < p.N ? bf16_bits_to_f32(__ldg(scales + n)) : 0.0f;
+                    nrp[r] = nrs.codes + static_cast<size_t>(nok[r] ? nl : 0) * p.row_words;
+                    snext[r] = n < p.N ? bf16_bits_to_f32(__ldg(nrs.scales + n)) : 0.0f;
                 }
                 load_block_group<KB, R>(nrp, nok, 0, lg, nw);
             } else {
@@ -572,12 +605,13 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 
             if (b_first == 0 && b + 1 == p.nblocks) {
                 // this CTA owns the whole K-range of the tile-group
+                const RowSrc rs = row_source<C>(p, codes, scales, out, row0);
 #pragma unroll
                 for (int j = 0; j < NV / 8; ++j) {
                     const int i = vbase + j;
                     const int r = i / MM, m = i - r * MM;
-                    if (i < R * MM && row0 + slot + 4 * r < p.N)
-                        out[static_cast<size_t>(m) * p.N + row0 + slot + 4 * r] = bf16_bits_rn(v[j]);
+                    const int n = row0 - rs.first + slot + 4 * r;
+                    if (i < R * MM && n < p.N) rs.out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(v[j]);
                 }
             } else {
                 // ---- split row: publish the partial now, take the ticket after the loop ----
@@ -672,7 +706,7 @@ constexpr size_t kCounterBytes = kCounterCapacity * sizeof(uint32_t);
 
 // Host-side planning.
 template <class C>
-SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev) {
+SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev, bool two = false) {
     SmallMPlan p{};
     p.M = C::MM;
     p.K = K;
@@ -681,6 +715,10 @@ SmallMPlan plan_smallm(int K, int N, int k, const DeviceInfo& dev) {
     p.row_words = K / 32 * k;
     const int rows_per_tg = C::WARPS * C::ROWS_PER_TILE;
     p.ntg = (N + rows_per_tg - 1) / rows_per_tg;
+    if (two) {   // the second matrix starts at the next whole tile-group
+        p.npad = p.ntg * rows_per_tg;
+        p.ntg *= 2;
+    }
     p.U = p.ntg * p.nblocks;
     int P = dev.num_sms * C::OCC;
     if (P > p.U) P = p.U;
@@ -706,8 +744,12 @@ bool smallm_fits_counters(const SmallMPlan& p) {
 template <class C, int KB>
 int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales,
                            int K, int N, uint16_t* out, void* ws, size_t ws_bytes,
-                           cudaStream_t stream, const DeviceInfo& dev) {
-    SmallMPlan p = plan_smallm<C>(K, N, KB, dev);
+                           cudaStream_t stream, const DeviceInfo& dev, const SecondMatrix& second = SecondMatrix{}) {
+    if ((second.codes != nullptr) != C::TWO) return -3;
+    SmallMPlan p = plan_smallm<C>(K, N, KB, dev, C::TWO);
+    p.codes2 = second.codes;
+    p.scales2 = second.scales;
+    p.out2 = second.out;
     if (!smallm_fits_counters<C>(p)) return -2;
     if (p.P >= (1 << 15)) return -3;   // CTA indices are packed in 15 bits (contributors_info)
     const size_t need = smallm_workspace_bytes<C>(p);
@@ -732,5 +774,11 @@ template <int KB>
 int launch_smallm_k(int M, const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K,
                     int N, uint16_t* out, void* ws, size_t ws_bytes, cudaStream_t stream,
                     const DeviceInfo& dev);
+
+// The same with a second matrix sharing x (instantiated in gemm_smallm2_k*.cu).
+template <int KB>
+int launch_smallm2_k(int M, const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K,
+                     int N, uint16_t* out, void* ws, size_t ws_bytes, cudaStream_t stream,
+                     const DeviceInfo& dev, const SecondMatrix& second);
 
 }  // namespace trellis

@@ -44,11 +44,24 @@ cudaError_t launch_programmatic(void (*kernel)(Params...), unsigned grid, unsign
 int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
                   uint16_t* out, cudaStream_t stream, const DeviceInfo& dev);
 
+// A second weight matrix [N, K] sharing x with the first (gate and up
+// projections), multiplied in the same launch; codes == nullptr: none.
+struct SecondMatrix {
+    const uint32_t* codes = nullptr;
+    const uint16_t* scales = nullptr;
+    uint16_t* out = nullptr;
+};
+
 // Fused decode-and-multiply for 1 <= M <= 16 (CUDA cores).
-size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo& dev);
+size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo& dev, bool two = false);
 int launch_gemm_smallm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M,
                        int K, int N, int k, uint16_t* out, void* workspace, size_t workspace_bytes,
-                       cudaStream_t stream, const DeviceInfo& dev);
+                       cudaStream_t stream, const DeviceInfo& dev, const SecondMatrix& second = SecondMatrix{});
+
+// act[i] = bf16(silu(g[i]) * u[i]) for count bf16 elements (silu(v) = v / (1 + e^-v),
+// in fp32 from the bf16 inputs).  Returns 0 or a trellis_status.
+int launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* act, size_t count, cudaStream_t stream,
+                    const DeviceInfo& dev);
 
 // Fused decode-and-multiply for M > 16 on the tensor cores (tcgen05), in
 // chunks of 64 activation rows.

@@ -188,6 +188,57 @@ int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scale
     return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, ws, need, stream, dev);
 }
 
+int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T, size_t* bytes) {
+    if (bytes == nullptr) return TRELLIS_ERR_NULL;
+    int rc = check_geometry(K, N, k, L, T);
+    if (rc != TRELLIS_OK) return rc;
+    if (!gemm_m_supported(M)) return TRELLIS_ERR_UNSUPPORTED;
+    if (gemm_on_tensor_cores(M)) {
+        *bytes = 0;
+        return TRELLIS_OK;
+    }
+    // both matrices' rows in one launch: twice the tile-groups (rounded)
+    if (static_cast<long long>(N) * 2 * (K / T) >= (1ll << 31)) return TRELLIS_ERR_SHAPE;
+    DeviceInfo dev;
+    rc = device_info(dev);
+    if (rc != TRELLIS_OK) return rc;
+    *bytes = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev, true);
+    return *bytes == 0 ? TRELLIS_ERR_SHAPE : TRELLIS_OK;
+}
+
+int trellis_gemm_gateup(const uint16_t* x, const uint32_t* codes_gate, const uint16_t* scales_gate,
+                        const uint32_t* codes_up, const uint16_t* scales_up, int M, int K, int N, int k, int L,
+                        int T, uint16_t* out_gate, uint16_t* out_up, uint16_t* out_act, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+    int rc = check_gemm(x, codes_gate, scales_gate, M, K, N, k, L, T, out_gate);
+    if (rc != TRELLIS_OK) return rc;
+    rc = check_gemm(x, codes_up, scales_up, M, K, N, k, L, T, out_up);
+    if (rc != TRELLIS_OK) return rc;
+    if (out_act != nullptr && !aligned(out_act, 2)) return TRELLIS_ERR_ALIGN;
+    size_t need = 0;
+    rc = trellis_gemm_gateup_workspace_size(M, K, N, k, L, T, &need);
+    if (rc != TRELLIS_OK) return rc;
+    DeviceInfo dev;
+    rc = device_info(dev);
+    if (rc != TRELLIS_OK) return rc;
+    if (gemm_on_tensor_cores(M)) {
+        rc = trellis::launch_gemm_tc(x, codes_gate, scales_gate, M, K, N, k, out_gate, stream);
+        if (rc == TRELLIS_OK) rc = trellis::launch_gemm_tc(x, codes_up, scales_up, M, K, N, k, out_up, stream);
+    } else {
+        if (workspace == nullptr || workspace_bytes < need) return TRELLIS_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return TRELLIS_ERR_ALIGN;
+        trellis::SecondMatrix up;
+        up.codes = codes_up;
+        up.scales = scales_up;
+        up.out = out_up;
+        rc = trellis::launch_gemm_smallm(x, codes_gate, scales_gate, M, K, N, k, out_gate, workspace,
+                                         workspace_bytes, stream, dev, up);
+    }
+    if (rc == TRELLIS_OK && out_act != nullptr)
+        rc = trellis::launch_silu_mul(out_gate, out_up, out_act, static_cast<size_t>(M) * N, stream, dev);
+    return rc;
+}
+
 int trellis_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return TRELLIS_ERR_CUDA;
     unsigned int flags = 0u;
