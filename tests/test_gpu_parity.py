@@ -104,12 +104,13 @@ def test_gemm_m64_tensor_cores(tq, oracle_lib, k, N, K):
     assert_gemm_close(got, ref, refabs, f"M=64 N={N} K={K} k={k}")
 
 
-@pytest.mark.parametrize("M", [17, 33, 63, 65, 100, 128, 200])
+@pytest.mark.parametrize("M", [17, 33, 63, 65, 100, 128, 129, 200, 256, 257, 300, 513])
 @pytest.mark.parametrize("k", [2, 4])
 def test_gemm_general_m_tensor_cores(tq, oracle_lib, M, k):
-    """M > 16 runs on tcgen05 in chunks of 64 activation rows; a partial chunk's
-    missing rows are zero-filled by the TMA and never stored: the rows after
-    the output (sentinel-filled) stay untouched."""
+    """M > 16 runs on tcgen05 with the MMA's N = 64, 128 or 256 (chunks of 256
+    rows above that, the last one overlapping); a partial chunk's missing rows
+    are zero-filled or never loaded and never stored: the rows after the output
+    (sentinel-filled) stay untouched."""
     import torch
     from trellis_quantized_weight_gb300 import binding
     N, K = 300, 512
@@ -130,9 +131,12 @@ def test_gemm_general_m_tensor_cores(tq, oracle_lib, M, k):
     assert_gemm_close(got, ref, refabs, f"M={M} N={N} K={K} k={k}")
 
 
-def test_gemm_m100_one_hot_is_exact(tq, oracle_lib):
-    """Across two 64-row chunks each row of x selects a weight column, bit for bit."""
-    N, K, k, M = 256, 1024, 3, 100
+@pytest.mark.parametrize("M", [100, 300])
+def test_gemm_one_hot_rows_are_exact(tq, oracle_lib, M):
+    """Each row of x selects a weight column, bit for bit: at M = 100 one
+    128-row launch with a partial tile, at M = 300 two overlapping 256-row
+    chunks."""
+    N, K, k = 256, 1024, 3
     _, codes, scales = _inputs(1, K, N, k, seed=642)
     w = oracle_lib.decode(codes, scales, K, N, k)
     cols = [(53 * i + 11) % K for i in range(M)]

@@ -1,29 +1,35 @@
-// Fused decode-and-multiply for M = 64 activation rows on the 5th-generation
+// Fused decode-and-multiply for M > 16 activation rows on the 5th-generation
 // tensor cores (tcgen05, sm_103a).
 //
 // What it computes is the same as the CUDA-core product (the wide-prefill
 // kernel on the page "mlx-bun 0.2.0 -> 0.4.0", trellis-wide-prefill.ts):
 // out[m, n] = bf16( sum_k w[n, k] * x[m, k] ) with w the decoded bf16 weights.
-// At M = 64 the multiply is a real dense contraction, so the decoded weights
-// go to the tensor cores instead of the FMA pipes:
+// With tens of activation rows the multiply is a real dense contraction, so
+// the decoded weights go to the tensor cores instead of the FMA pipes:
 //
-//   D[n, m] (TMEM, fp32, 128 lanes x 64 columns) += A[n, k] * B[m, k]^T
+//   D[n, m] (TMEM, fp32, 128 lanes x NB columns) += A[n, k] * B[m, k]^T
 //   A = decoded weight tile, 128 rows x 16 k, bf16, K-major, shared memory
-//   B = activation tile,      64 rows x 16 k, bf16, K-major, shared memory
+//   B = activation tile,      NB rows x 16 k, bf16, K-major, shared memory
 //
+// NB (the MMA's N) is 64, 128 or 256: one launch serves up to NB activation
+// rows, and larger M runs in NB-row chunks, each decoding the weights again.
 // One CTA owns 128 weight rows and the whole K range.  Its warps:
 //   * 16 decode warps write the bf16 weights of one 128-k stage into shared
-//     memory in the canonical K-major layout (8-row x 16-byte core matrices,
-//     no swizzle); lanes of one shared-memory phase write 8 different rows,
-//     so the stores are conflict-free.  The quotient is looked up in a
-//     per-lane shared-memory table (conflict-free, see trellis_device.cuh).
-//   * 1 TMA warp loads the activation tile of the stage with 3-D tensor copies
-//     that land directly in the same core-matrix layout.
+//     memory in the K-major 128-byte-swizzled layout: two k-blocks of 64 k,
+//     each row of a k-block 128 bytes, and inside every 8-row (1 KB) atom the
+//     16-byte chunk c of row r stored at chunk c ^ r.  The 8 lanes of one
+//     shared-memory phase write 8 different rows, so the XOR spreads their
+//     16-byte stores over all 32 banks.  The quotient comes from the ALU form
+//     of the residual correction (trellis_device.cuh).
+//   * 1 TMA warp loads the activation tile of the stage with two 2-D tensor
+//     copies (one per k-block, 128-byte rows) that the TMA swizzles into the
+//     same layout.  The box covers the chunk's rows rounded up to 8; rows
+//     beyond it only feed accumulator columns that are never stored.
 //   * 1 MMA warp: one thread issues the 8 tcgen05.mma (K = 16 each) of a stage
 //     and commits them to the stage's "empty" barrier.
-// Four stages are in flight (mbarrier full/empty pairs).  After the last stage
-// the decode warps read the accumulator back with tcgen05.ld, round to bf16
-// and store out[m, n] (each store instruction writes 32 consecutive n).
+// Two to four stages are in flight (mbarrier full/empty pairs).  After the
+// last stage the decode warps read the accumulator back with tcgen05.ld, round
+// to bf16 and store out[m, n] (each store instruction writes 32 consecutive n).
 //
 // Every mbarrier wait is bounded; a wait that runs out records an error in a
 // device word (read by trellis_device_status) and the CTA winds down.
@@ -41,34 +47,54 @@ __device__ unsigned int g_tc_error = 0u;
 namespace {
 
 constexpr int kTcRows = 128;                 // weight rows per CTA (MMA M)
-constexpr int kTcM = 64;                     // activation rows (MMA N)
 constexpr int kTcStageK = 128;               // k per pipeline stage
-constexpr int kTcStages = 4;
 constexpr int kTcDecodeWarps = 16;
 constexpr int kTcThreads = (kTcDecodeWarps + 2) * 32;
 constexpr int kTcTmaWarp = kTcDecodeWarps;
 constexpr int kTcMmaWarp = kTcDecodeWarps + 1;
-constexpr int kTcTmemCols = 64;
 
-// Quotient by the per-lane table (one shared load) or by the three-op
-// residual correction (ALU only).  This kernel's shared-memory pipe is busy
-// with the A tiles, the activation tiles and the tensor cores' operand reads,
-// while its issue slots are not, so the ALU form is used and the table's
-// shared memory goes to deeper pipelining instead.
-constexpr bool kTcLut = false;
-constexpr int kTableRegion = kTcLut ? (kQuotientTableBytes + 1023) / 1024 * 1024 : 0;
+// The quotient uses the three-op residual correction (ALU only), not the
+// per-lane shared-memory table of the CUDA-core kernel: this kernel's
+// shared-memory pipe carries the A tiles, the activation tiles and the tensor
+// cores' operand reads, while its issue slots have room, and the table's
+// 113 KB of shared memory goes to deeper pipelining instead.
 
 constexpr int kABytes = kTcRows * kTcStageK * 2;     // 32 KB
-constexpr int kBBytes = kTcM * kTcStageK * 2;        // 16 KB
-constexpr int kCoreSBO = (kTcStageK / 8) * 128;      // bytes between 8-row groups: 2 KB
-constexpr int kCoreLBO = 128;                        // bytes between k-adjacent core matrices
+constexpr int kSwK = 64;                             // k per 128-byte swizzled row (one k-block)
+constexpr int kSwRowBytes = kSwK * 2;                // 128
+constexpr int kSwAtomBytes = 8 * kSwRowBytes;        // 8-row atom: 1 KB, the stride between 8-row groups
+constexpr int kAKBlockBytes = kTcRows * kSwRowBytes; // 16 KB
 
-constexpr int kOffA = kTableRegion;
-constexpr int kOffB = kOffA + kTcStages * kABytes;
-constexpr int kOffBar = kOffB + kTcStages * kBBytes;
-constexpr int kBarFull = 0, kBarEmpty = kTcStages, kBarDone = 2 * kTcStages;
-constexpr int kOffTaddr = kOffBar + (2 * kTcStages + 1) * 8;
-constexpr int kTcSmemBytes = kOffTaddr + 16;
+// Activation rows a chunk of M rows loads per k-block: M rounded up to 8, at
+// most NB (the TMA box height).
+__host__ __device__ constexpr int tc_box_rows(int M, int NB) { return ((M + 7) & ~7) < NB ? ((M + 7) & ~7) : NB; }
+
+// One pass multiplies the decoded weights by NB activation rows (the MMA's N:
+// 64, 128 or 256), so a weight tile is decoded once per NB rows of x.  Stages
+// in flight fill about 192 KB of shared memory: 4 at NB = 64, 3 at 128, 2 at
+// 256 (each stage: a 32 KB weight tile and an NB x 128 activation tile).
+template <int NB>
+struct TcShape {
+    static constexpr int kStages = NB == 64 ? 4 : (NB == 128 ? 3 : 2);
+    static constexpr int kBBytes = NB * kTcStageK * 2;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kABytes;
+    static constexpr int kOffBar = kOffB + kStages * kBBytes;
+    static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarDone = 2 * kStages;
+    static constexpr int kOffTaddr = kOffBar + (2 * kStages + 1) * 8;
+    // + 1 KB so that the base can be rounded up to the 1 KB the swizzle atoms need
+    static constexpr int kSmemBytes = kOffTaddr + 16 + 1024;
+    static constexpr int kTmemCols = NB;   // fp32 accumulator: 128 lanes x NB columns
+    // instruction descriptor: kind::f16, D fp32, A and B bf16, both K-major,
+    // N = NB (bits 17-22: N/8), M = 128 (bits 24-28: M/16)
+    static constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                           (static_cast<uint32_t>(NB >> 3) << 17) |
+                                           (static_cast<uint32_t>(kTcRows >> 4) << 24);
+    static_assert(NB == 64 || NB == 128 || NB == 256, "MMA N");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
+    static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kBBytes % 1024 == 0 && kABytes % 1024 == 0,
+                  "swizzle atoms must start on 1 KB boundaries");
+};
 
 constexpr uint32_t kWaitLimit = 1u << 24;   // polls before a wait gives up
 
@@ -101,43 +127,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
 }
-// Shared-memory matrix descriptor: no swizzle, K-major core matrices.
+// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: start
+// address, leading offset unused by this layout (encoded 1), stride between
+// 8-row atoms 1 KB, descriptor version 1 (bit 46), swizzle mode 2 (bits
+// 61-63).  A k step of 16 inside an atom advances the start by 32 bytes: the
+// swizzle is applied to the final address bits, as the stores applied it.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
     return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
-           (static_cast<uint64_t>(kCoreLBO >> 4) << 16) |
-           (static_cast<uint64_t>(kCoreSBO >> 4) << 32) |
-           (1ull << 46);                       // descriptor version for tcgen05
+           (1ull << 16) |
+           (static_cast<uint64_t>(kSwAtomBytes >> 4) << 32) |
+           (1ull << 46) |
+           (2ull << 61);
 }
-// Instruction descriptor: kind::f16, D fp32, A and B bf16, both K-major,
-// N = 64, M = 128.
-constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                (static_cast<uint32_t>(kTcM >> 3) << 17) |
-                                (static_cast<uint32_t>(kTcRows >> 4) << 24);
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                  " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(kInstrDesc), "r"(accumulate) : "memory");
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ float tc_quotient(uint32_t win, uint32_t lane_base) {
-    const uint32_t z = win * kHashMul + kHashAdd;
-    const uint32_t addr = __dp4a(z, 0x80808080u, lane_base);
-    float v;
-    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
 }
 
 template <int KB>
@@ -166,14 +183,21 @@ __device__ __forceinline__ void tc_load_group(const uint32_t* __restrict__ row_c
     }
 }
 
-template <int KB>
+template <int KB, int NB>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
                uint16_t* __restrict__ out, int M, int K, int N, int row_words,
                const __grid_constant__ CUtensorMap x_map) {
-    extern __shared__ __align__(1024) unsigned char smem[];
+    using S = TcShape<NB>;
+    constexpr int kTcStages = S::kStages;
+    constexpr int kBBytes = S::kBBytes;
+    constexpr int kOffA = S::kOffA, kOffB = S::kOffB, kOffBar = S::kOffBar, kOffTaddr = S::kOffTaddr;
+    constexpr int kBarFull = S::kBarFull, kBarEmpty = S::kBarEmpty, kBarDone = S::kBarDone;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const uint32_t sraw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    const uint32_t sbase = (sraw + 1023u) & ~1023u;
+    unsigned char* const smem = smem_raw + (sbase - sraw);
     const uint32_t bar_full = sbase + kOffBar + 8 * kBarFull;
     const uint32_t bar_empty = sbase + kOffBar + 8 * kBarEmpty;
     const uint32_t bar_done = sbase + kOffBar + 8 * kBarDone;
@@ -191,11 +215,8 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
     }
     if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     :: "r"(sbase + kOffTaddr), "r"(kTcTmemCols) : "memory");
+                     :: "r"(sbase + kOffTaddr), "r"(S::kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    if (kTcLut && warp < kTcDecodeWarps) {
-        build_quotient_table(reinterpret_cast<float*>(smem), threadIdx.x, kTcDecodeWarps * 32);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -213,11 +234,12 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         const float sr = ok ? bf16_bits_to_f32(__ldg(scales + row)) : 0.0f;
         const float2 s2 = make_float2(sr, sr);
         const uint32_t* row_codes = codes + static_cast<size_t>(ok ? row : 0) * row_words;
-        const uint32_t lane_tbl = quotient_table_lane_address(smem, lane);
         const int src_lane = (gi == 0) ? lane : lane - 8;
-        // this thread's 4 core-matrix rows inside a stage's A tile
-        const uint32_t a_row_off = static_cast<uint32_t>((row_local >> 3) * kCoreSBO + gi * 4 * kCoreLBO +
-                                                         (row_local & 7) * 16);
+        // this thread's 64 bytes (k = 32*gi .. 32*gi+31) inside a stage's A
+        // tile: k-block gi/2, 16-byte chunks 4*(gi%2) + q, swizzled by row
+        const uint32_t a_row_off = static_cast<uint32_t>((gi >> 1) * kAKBlockBytes + row_local * kSwRowBytes);
+        const uint32_t a_chunk0 = static_cast<uint32_t>(4 * (gi & 1));
+        const uint32_t a_rsw = static_cast<uint32_t>(row_local & 7);
         // code words travel through a 4-deep register ring: stage i+3 is
         // loaded while stage i is decoded (ring indices are compile-time
         // because the stage loop is unrolled by the ring depth)
@@ -253,14 +275,8 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                 uint32_t packed[16];
 #pragma unroll
                 for (int jp = 0; jp < 16; ++jp) {
-                    float2 v;
-                    if constexpr (kTcLut) {
-                        v = make_float2(tc_quotient(group_window<KB>(w, 2 * jp), lane_tbl),
-                                        tc_quotient(group_window<KB>(w, 2 * jp + 1), lane_tbl));
-                    } else {
-                        v = make_float2(window_value(group_window<KB>(w, 2 * jp)),
-                                        window_value(group_window<KB>(w, 2 * jp + 1)));
-                    }
+                    const float2 v = make_float2(window_value(group_window<KB>(w, 2 * jp)),
+                                                 window_value(group_window<KB>(w, 2 * jp + 1)));
                     const float2 ws = __fmul2_rn(v, s2);
                     packed[jp] = pack_bf16x2(ws.x, ws.y);
                 }
@@ -270,8 +286,9 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 :: "r"(dst + q * kCoreLBO), "r"(packed[4 * q]), "r"(packed[4 * q + 1]),
-                                    "r"(packed[4 * q + 2]), "r"(packed[4 * q + 3]) : "memory");
+                                 :: "r"(dst + (((a_chunk0 + q) ^ a_rsw) << 4)), "r"(packed[4 * q]),
+                                    "r"(packed[4 * q + 1]), "r"(packed[4 * q + 2]), "r"(packed[4 * q + 3])
+                                 : "memory");
                 fence_async_shared();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_full + 8 * s);
@@ -281,10 +298,14 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         // -------------------------------------------------------------- epilogue
         const bool done = alive && mbar_wait(bar_done, 0);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (done) {
-            const int sub = warp & 3, colq = warp >> 2;
+        // warp w reads TMEM lanes 32*(w%4) .. +31 (its weight rows) and the
+        // columns (activation rows) of quarter w/4, 16 at a time
+        const int sub = warp & 3, colq = warp >> 2;
+#pragma unroll
+        for (int cc = 0; cc < NB / 64 && done; ++cc) {
+            const int col = colq * (NB / 4) + 16 * cc;
             uint32_t r[16];
-            const uint32_t ta = taddr + (static_cast<uint32_t>(32 * sub) << 16) + static_cast<uint32_t>(16 * colq);
+            const uint32_t ta = taddr + (static_cast<uint32_t>(32 * sub) << 16) + static_cast<uint32_t>(col);
             asm volatile(
                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
                 "%12, %13, %14, %15}, [%16];"
@@ -298,21 +319,25 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                 // activation rows m >= M were zero-filled by the TMA; not stored
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    if (16 * colq + j < M)
-                        out[static_cast<size_t>(16 * colq + j) * N + n] = bf16_bits_rn(__uint_as_float(r[j]));
+                    if (col + j < M)
+                        out[static_cast<size_t>(col + j) * N + n] = bf16_bits_rn(__uint_as_float(r[j]));
             }
         }
     } else if (warp == kTcTmaWarp) {
         // ------------------------------------------------------------- x via TMA
         if (lane == 0) {
+            // one box per k-block: the chunk's rows rounded up to 8 (rows past
+            // M zero-filled by the TMA) x 64 k, 128 bytes a row
+            const int rows = tc_box_rows(M, NB);
             for (int i = 0; i < nstages; ++i) {
                 const int s = i % kTcStages;
                 if (i >= kTcStages && !mbar_wait(bar_empty + 8 * s, ((i / kTcStages) + 1) & 1)) break;
-                mbar_arrive_expect_tx(bar_full + 8 * s, kBBytes);
+                mbar_arrive_expect_tx(bar_full + 8 * s, static_cast<uint32_t>(2 * rows * kSwRowBytes));
                 const uint32_t dst = sbase + kOffB + s * kBBytes;
 #pragma unroll
-                for (int mg = 0; mg < kTcM / 8; ++mg)
-                    tma_load_3d(dst + mg * kCoreSBO, &x_map, 0, 8 * mg, i * (kTcStageK / 8), bar_full + 8 * s);
+                for (int kb = 0; kb < kTcStageK / kSwK; ++kb)
+                    tma_load_2d(dst + kb * (NB * kSwRowBytes), &x_map, i * kTcStageK + kb * kSwK, 0,
+                                bar_full + 8 * s);
             }
         }
     } else {
@@ -326,9 +351,12 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                 const uint32_t a0 = sbase + kOffA + s * kABytes;
                 const uint32_t b0 = sbase + kOffB + s * kBBytes;
 #pragma unroll
-                for (int kk = 0; kk < kTcStageK / 16; ++kk)
-                    mma_bf16(taddr, smem_desc(a0 + kk * 2 * kCoreLBO), smem_desc(b0 + kk * 2 * kCoreLBO),
+                for (int kk = 0; kk < kTcStageK / 16; ++kk) {
+                    const int kb = kk / (kSwK / 16), ks = kk % (kSwK / 16);
+                    mma_bf16(taddr, smem_desc(a0 + kb * kAKBlockBytes + ks * 32),
+                             smem_desc(b0 + kb * (NB * kSwRowBytes) + ks * 32), S::kInstrDesc,
                              (i > 0 || kk > 0) ? 1u : 0u);
+                }
                 mma_commit(bar_empty + 8 * s);
             }
             mma_commit(bar_done);   // tracks every MMA issued above
@@ -341,7 +369,7 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
     __syncthreads();
     if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(kTcTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(S::kTmemCols)
                      : "memory");
     }
 }
@@ -364,54 +392,59 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// x [M, K] bf16 row-major (M <= 64 rows of this chunk) seen as a 3-D tensor
-// (8 k, m, K/8): a box of (8, 8, 16) is one 8-row group of 16 k-adjacent core
-// matrices, laid out in shared memory exactly as the MMA's K-major no-swizzle
-// operand.  Rows m >= M of the 64-row tile lie outside the tensor and are
-// filled with zeros.
-bool make_x_map(CUtensorMap* map, const uint16_t* x, int M, int K) {
+// x [M, K] bf16 row-major (the M <= NB rows of this chunk) as a 2-D tensor
+// (k, m) with a box of 64 k (128 bytes) x `rows` rows, swizzled by the TMA
+// into the MMA's K-major 128-byte-swizzle layout.  Box rows m >= M lie outside
+// the tensor and are filled with zeros.
+bool make_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
-    const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 8)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 16};
-    const cuuint32_t box[3] = {8, 8, kTcStageK / 8};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(x), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {kSwK, static_cast<cuuint32_t>(rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One launch per chunk of 64 activation rows (each chunk decodes the weights
-// again; the launches are programmatically chained on the stream).  Only
-// M < 64 runs a partial chunk; for larger M the last chunk is moved back to end
-// at row M, so it is full and overlaps the one before: the overlapping rows are
-// computed again with identical bits (each output is its own dot product) and
-// written again after the earlier launch (stream order).  A chunk of very few
-// rows would make most of the TMA box fall outside the tensor, which measured
-// several times slower.
-template <int KB>
-int launch_tc_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
-                       uint16_t* out, cudaStream_t stream) {
+template <int KB, int NB>
+int launch_tc_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
+                     uint16_t* out, cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_tc_kernel<KB, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcShape<NB>::kSmemBytes) != cudaSuccess)
             return -5;
         attr_set = true;
     }
     const int grid = (N + kTcRows - 1) / kTcRows;
-    for (int m = 0; m < M; m += kTcM) {
-        const int m0 = (M > kTcM && m + kTcM > M) ? M - kTcM : m;
-        const int mc = (M - m0) < kTcM ? (M - m0) : kTcM;
+    for (int m = 0; m < M; m += NB) {
+        const int m0 = (M > NB && m + NB > M) ? M - NB : m;
+        const int mc = (M - m0) < NB ? (M - m0) : NB;
         CUtensorMap map;
-        if (!make_x_map(&map, x + static_cast<size_t>(m0) * K, mc, K)) return -5;
-        const cudaError_t e = launch_programmatic(gemm_tc_kernel<KB>, static_cast<unsigned>(grid),
-                                                  static_cast<unsigned>(kTcThreads), kTcSmemBytes, stream,
-                                                  codes, scales, out + static_cast<size_t>(m0) * N, mc, K, N,
-                                                  K / 32 * KB, map);
+        if (!make_x_map(&map, x + static_cast<size_t>(m0) * K, mc, K, tc_box_rows(mc, NB))) return -5;
+        const cudaError_t e = launch_programmatic(gemm_tc_kernel<KB, NB>, static_cast<unsigned>(grid),
+                                                  static_cast<unsigned>(kTcThreads), TcShape<NB>::kSmemBytes,
+                                                  stream, codes, scales, out + static_cast<size_t>(m0) * N, mc, K,
+                                                  N, K / 32 * KB, map);
         if (e != cudaSuccess) return -5;
     }
     return 0;
+}
+
+// The MMA's N follows M: 64 for M <= 64, 128 for M <= 128, else 256.  Above
+// 256 rows the launches take 256-row chunks (each decodes the weights again;
+// they are programmatically chained on the stream), and the last chunk is
+// moved back to end at row M, so it is full and overlaps the one before: the
+// overlapping rows are computed again with identical bits (each output is its
+// own dot product) and written again after the earlier launch (stream order).
+template <int KB>
+int launch_tc_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
+                       uint16_t* out, cudaStream_t stream) {
+    if (M <= 64) return launch_tc_chunks<KB, 64>(x, codes, scales, M, K, N, out, stream);
+    if (M <= 128) return launch_tc_chunks<KB, 128>(x, codes, scales, M, K, N, out, stream);
+    return launch_tc_chunks<KB, 256>(x, codes, scales, M, K, N, out, stream);
 }
 
 }  // namespace
