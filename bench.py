@@ -444,9 +444,10 @@ def run_ours(args, wl):
                "sample": f"{rows} rows x K={wl.K} of {wl.name} (decode + product), {dt:.1f} s wall"}
 
     value = whole_job_gbs(world, n_mats * wl.code_bytes, ms_step)
-    # our kernels per step: one per 64-row chunk per matrix on the tensor cores,
-    # else one small-M launch; plus the gate/up activation
-    chunks = (wl.M + 63) // 64 if wl.M > 16 and args.entry != "decode" else 1
+    # our kernels per step: on the tensor cores one launch per matrix for M <= 256,
+    # else one per 256-row chunk; otherwise one small-M launch; plus the gate/up
+    # activation
+    chunks = max(1, (wl.M + 255) // 256) if wl.M > 16 and args.entry != "decode" else 1
     launches_per_step = n_mats * chunks if wl.M > 16 and args.entry != "decode" else 1
     if args.entry == "gateup":
         launches_per_step += 1

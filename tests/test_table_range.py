@@ -29,3 +29,28 @@ def test_reachable_byte_sums_match_table_range():
         sums.add((p & 0xFFFF) + (p >> 16))
     assert min(sums) == lo and max(sums) == hi
     assert hi - lo + 1 == 903
+
+
+def _float_const(name: str) -> float:
+    m = re.search(rf"constexpr\s+float\s+{name}\s*=\s*(0x[0-9a-fA-F.]+p[-+]?\d+)f;", HEADER.read_text())
+    assert m, f"{name} not found in {HEADER.name}"
+    return float.fromhex(m.group(1))
+
+
+def test_two_part_reciprocal_rounds_every_code_correctly():
+    """The kernels compute value = fma(code, kRecipLo, code * kRecipHi) in fp32.
+    Checked here for every code in [-510, 510] with exact rationals: the product
+    code * kRecipHi is exact, and the FMA's single rounding of
+    code * kRecipLo + code * kRecipHi gives the fp32 nearest to code / c."""
+    import sys
+    sys.path.insert(0, str(pathlib.Path(__file__).resolve().parent))
+    from fractions import Fraction
+    import pins
+    hi, lo = Fraction(_float_const("kRecipHi")), Fraction(_float_const("kRecipLo"))
+    assert hi.numerator < (1 << 14) and (hi.denominator & (hi.denominator - 1)) == 0, "kRecipHi: 14 bits"
+    assert Fraction(float(pins.rn_f32(1 / pins.C_DIV - hi))) == lo, "kRecipLo is fp32(1/c - kRecipHi)"
+    for code in range(-510, 511):
+        prod = code * hi
+        assert Fraction(float(pins.rn_f32(prod))) == prod, code
+        got = pins.rn_f32(code * lo + prod)
+        assert got == pins.value_exact(code), code

@@ -89,9 +89,9 @@ decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ s
         uint32_t packed[16];
 #pragma unroll
         for (int jp = 0; jp < 16; ++jp) {
-            const float a = __fmul_rn(window_value(group_window<KB>(w, 2 * jp)), cs);
-            const float b = __fmul_rn(window_value(group_window<KB>(w, 2 * jp + 1)), cs);
-            packed[jp] = pack_bf16x2(a, b);
+            const float2 v = __fmul2_rn(window_value2(group_window<KB>(w, 2 * jp), group_window<KB>(w, 2 * jp + 1)),
+                                        make_float2(cs, cs));
+            packed[jp] = pack_bf16x2(v.x, v.y);
         }
 
         // The bulk copy issued two steps ago from this buffer must have read it.

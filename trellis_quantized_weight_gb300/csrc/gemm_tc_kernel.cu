@@ -275,8 +275,7 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                 uint32_t packed[16];
 #pragma unroll
                 for (int jp = 0; jp < 16; ++jp) {
-                    const float2 v = make_float2(window_value(group_window<KB>(w, 2 * jp)),
-                                                 window_value(group_window<KB>(w, 2 * jp + 1)));
+                    const float2 v = window_value2(group_window<KB>(w, 2 * jp), group_window<KB>(w, 2 * jp + 1));
                     const float2 ws = __fmul2_rn(v, s2);
                     packed[jp] = pack_bf16x2(ws.x, ws.y);
                 }

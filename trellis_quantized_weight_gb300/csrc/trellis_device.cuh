@@ -26,8 +26,6 @@ constexpr int kGroupsPerBlock = kT / 32;
 
 constexpr uint32_t kHashMul = 34038481u;
 constexpr uint32_t kHashAdd = 76625530u;
-constexpr float kDivisor = 147.800537109375f;
-constexpr float kRecip = 1.0f / 147.800537109375f;   // fp32 round-to-nearest of 1/c
 // dp4a(z, 0x01010101, 0x4B400000) is the bit pattern of the float
 // 1.5*2^23 + (byte sum), exactly; subtracting 1.5*2^23 + 510 leaves
 // float(code) exactly (both operands share the exponent 2^23, unit ulp).
@@ -49,14 +47,21 @@ __device__ __forceinline__ uint32_t group_window(const uint32_t (&w)[KB + 1], in
     return win & ((1u << kL) - 1u);
 }
 
-// float(code) -> code / 147.800537109375 rounded to nearest fp32, by the
-// page's residual correction: q0 = code*r, e = code - q0*c (exact in one FMA),
-// q = q0 + e*r.  For every integer code in [-510, 510] this is the correctly
-// rounded quotient (checked exhaustively against exact rational arithmetic).
+// float(code) -> code / 147.800537109375 rounded to nearest fp32, as a
+// multiplication by the reciprocal held in two fp32 parts (the double-word
+// constant multiplication of Brisebarre and Muller, "Correctly rounded
+// multiplication by arbitrary precision constants", IEEE TC 2008):
+// kRecipHi is 1/c to 14 significant bits (14189 * 2^-21), so code * kRecipHi
+// is exact for |code| <= 510 (at most 23 bits), and kRecipLo is the fp32 of
+// 1/c - kRecipHi.  One FMA adds code * kRecipLo to the exact product before
+// its only rounding.  For every integer code in [-510, 510] the result is the
+// correctly rounded quotient; the host tests check each code against exact
+// rational arithmetic, reading these two constants from this file.
+constexpr float kRecipHi = 0x1.bb68p-8f;
+constexpr float kRecipLo = 0x1.1a16f2p-25f;
+
 __device__ __forceinline__ float code_to_value(float code) {
-    const float approx = __fmul_rn(code, kRecip);
-    const float residual = __fmaf_rn(-approx, kDivisor, code);
-    return __fmaf_rn(residual, kRecip, approx);
+    return __fmaf_rn(code, kRecipLo, __fmul_rn(code, kRecipHi));
 }
 
 // 12-bit window -> fp32 value, bit-exact with code / 147.800537109375.
@@ -64,6 +69,17 @@ __device__ __forceinline__ float window_value(uint32_t win) {
     const uint32_t z = win * kHashMul + kHashAdd;
     const float biased = __uint_as_float(__dp4a(z, 0x01010101u, kMagicBits));
     return code_to_value(__fsub_rn(biased, kMagicPlusBias));
+}
+
+// Two windows at once: the same steps, the fp32 ones as paired (f32x2)
+// instructions, so each issue slot serves two weights.
+__device__ __forceinline__ float2 window_value2(uint32_t wa, uint32_t wb) {
+    const uint32_t za = wa * kHashMul + kHashAdd;
+    const uint32_t zb = wb * kHashMul + kHashAdd;
+    const float2 biased = make_float2(__uint_as_float(__dp4a(za, 0x01010101u, kMagicBits)),
+                                      __uint_as_float(__dp4a(zb, 0x01010101u, kMagicBits)));
+    const float2 code = __fadd2_rn(biased, make_float2(-kMagicPlusBias, -kMagicPlusBias));
+    return __ffma2_rn(code, make_float2(kRecipLo, kRecipLo), __fmul2_rn(code, make_float2(kRecipHi, kRecipHi)));
 }
 
 // ---- programmatic dependent launch --------------------------------------------
