@@ -1,7 +1,7 @@
 """Benchmark of the packed-Trellis decode-and-multiply on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--entry gemm|decode|gateup] [--rows M]
 
 One step = one fused decode-and-multiply call (trellis_gemm: code fetch,
 window, hash, quotient, scale/bf16 round, M-row FMA, reduction and bf16 store)
@@ -24,6 +24,7 @@ on a bounded sample of the same workload; it is a deliberately slow baseline.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import concurrent.futures as cf
 import glob
 import hashlib
@@ -536,11 +537,18 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds for the reference arm's timed run")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="activation rows M instead of the workload's own (a prefill sweep of the same weights)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     from trellis_quantized_weight_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
+    if args.rows is not None:
+        if not 1 <= args.rows <= 65536:
+            ap.error("--rows must be in 1..65536")
+        kind = "gemv" if args.rows == 1 else ("gemm" if args.rows <= 16 else "prefill")
+        wl = dataclasses.replace(wl, M=args.rows, name=f"{kind}_m{args.rows}_k{wl.K}_n{wl.N}_k{wl.k}")
     if args.impl == "reference":
         run_reference(args, wl)
     else:
