@@ -39,7 +39,7 @@
 //    The sum order is fixed: identical inputs give identical bits.  No CTA
 //    ever waits on another.
 //  * Decode per weight: funnel shift + mask, hash IMAD, then either the dp4a
-//    byte sum into a float and the 3-op residual-corrected quotient, or one
+//    byte sum into a float and the two-op quotient (trellis_device.cuh), or one
 //    dp4a that turns the hash into the address of the quotient in a per-lane
 //    shared-memory table (one conflict-free load).  Then a packed f32x2 scale
 //    multiply, a bf16 round that keeps fp32 format, and MM packed f32x2 FMAs
@@ -78,7 +78,7 @@ struct SmallMPlan {
 //   R      rows per lane (a warp's tile is 4*R rows)
 //   WARPS  warps per CTA (= tiles per tile-group)
 //   LUT    decode the quotient through a shared-memory table instead of the
-//          three-op residual correction (same bits either way)
+//          two-part reciprocal multiply (same bits either way)
 //   OCC    CTAs per SM
 //   UB     blocks staged per CTA barrier
 //   GM     group-major lane order (see the mapping notes above)

@@ -19,8 +19,9 @@
 //     each row of a k-block 128 bytes, and inside every 8-row (1 KB) atom the
 //     16-byte chunk c of row r stored at chunk c ^ r.  The 8 lanes of one
 //     shared-memory phase write 8 different rows, so the XOR spreads their
-//     16-byte stores over all 32 banks.  The quotient comes from the ALU form
-//     of the residual correction (trellis_device.cuh).
+//     16-byte stores over all 32 banks.  The quotient is computed on the FMA
+//     pipe (two-part reciprocal, two windows per f32x2 instruction;
+//     trellis_device.cuh).
 //   * 1 TMA warp loads the activation tile of the stage with two 2-D tensor
 //     copies (one per k-block, 128-byte rows) that the TMA swizzles into the
 //     same layout.  The box covers the chunk's rows rounded up to 8; rows
@@ -53,8 +54,8 @@ constexpr int kTcThreads = (kTcDecodeWarps + 2) * 32;
 constexpr int kTcTmaWarp = kTcDecodeWarps;
 constexpr int kTcMmaWarp = kTcDecodeWarps + 1;
 
-// The quotient uses the three-op residual correction (ALU only), not the
-// per-lane shared-memory table of the CUDA-core kernel: this kernel's
+// The quotient is computed (window_value2), not read from the per-lane
+// shared-memory table of the CUDA-core kernel: this kernel's
 // shared-memory pipe carries the A tiles, the activation tiles and the tensor
 // cores' operand reads, while its issue slots have room, and the table's
 // 113 KB of shared memory goes to deeper pipelining instead.

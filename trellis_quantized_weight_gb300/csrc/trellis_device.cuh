@@ -3,8 +3,10 @@
 // The per-weight arithmetic follows the wide-prefill Metal kernel on the page
 // "mlx-bun 0.2.0 -> 0.4.0" (package/src/model/trellis-wide-prefill.ts): an
 // L-bit window of the block's bit-string, the multiply-add hash, the sum of the
-// hash's four bytes minus 510, the residual-corrected fp32 quotient by
-// 147.800537109375, the per-row scale and a round to bf16.
+// hash's four bytes minus 510, the correctly rounded fp32 quotient by
+// 147.800537109375 (the page reaches it with a residual correction; here a
+// two-part reciprocal gives the same bits, see code_to_value), the per-row
+// scale and a round to bf16.
 //
 // Work is organised in "groups" of 32 consecutive weights of one block
 // (T = 256 weights, so 8 groups per block).  Group g holds weights
