@@ -26,9 +26,12 @@
  * rounded) -> w = bf16_rne(value * scale).  The product accumulates
  * float(w)*float(x) in fp32 and rounds each output once to bf16 (nearest even).
  *
- * Accepted geometry: k in {2, 3, 4}, L == 12, T == 256, K a positive multiple
- * of T, N >= 1, and for trellis_gemm 1 <= M <= 65536 (M <= 16 on the CUDA
- * cores, larger M on the tensor cores).  Anything else returns
+ * Accepted geometry: T == 256, 1 <= k <= 8, k < L <= 24, K a positive
+ * multiple of T, N >= 1, and for trellis_gemm 1 <= M <= 65536 (M <= 16 on the
+ * CUDA cores, larger M on the tensor cores).  The page's wrapper accepts
+ * k in {2, 3, 4} with L == 12; those geometries run on kernels specialised for
+ * them, the rest on kernels that take the window width at run time (same
+ * definition, same bits; slower).  Anything else returns
  * TRELLIS_ERR_UNSUPPORTED or TRELLIS_ERR_SHAPE before any launch.
  *
  * Every call is asynchronous on `stream` (0 = the legacy default stream): it

@@ -41,13 +41,13 @@ def _threads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
 
-def oracle_decode_par(o, codes, scales, K, N, k, rows=None):
+def oracle_decode_par(o, codes, scales, K, N, k, rows=None, L=12):
     n0, n1 = rows if rows is not None else (0, N)
     nt = _threads()
     edges = np.linspace(n0, n1, nt + 1).astype(int)
     parts = [(int(a), int(b)) for a, b in zip(edges[:-1], edges[1:]) if b > a]
     with cf.ThreadPoolExecutor(nt) as ex:
-        outs = list(ex.map(lambda r: o.decode(codes, scales, K, N, k, rows=r), parts))
+        outs = list(ex.map(lambda r: o.decode(codes, scales, K, N, k, L=L, rows=r), parts))
     return np.concatenate(outs, axis=0) if outs else np.empty((0, K), np.uint16)
 
 

@@ -41,16 +41,19 @@ def test_abi_version_and_status_strings(lib):
     assert lib.trellis_status_string(123).decode() == "TRELLIS_ERR_UNKNOWN"
 
 
-FAKE = 0x10000   # never dereferenced: every case below fails validation first
+FAKE = 0x10000   # never dereferenced: every case below fails validation first (a call that could
+                 # pass validation must use real device buffers)
 
 
 @pytest.mark.parametrize("args,want", [
     ((0, FAKE, 5120, 8, 4, 12, 256, FAKE, None), -1),          # NULL codes
     ((FAKE, 0, 5120, 8, 4, 12, 256, FAKE, None), -1),          # NULL scales
     ((FAKE, FAKE, 5120, 8, 4, 12, 256, 0, None), -1),          # NULL out
-    ((FAKE, FAKE, 5120, 8, 5, 12, 256, FAKE, None), -3),       # k = 5
-    ((FAKE, FAKE, 5120, 8, 1, 12, 256, FAKE, None), -3),       # k = 1
-    ((FAKE, FAKE, 5120, 8, 4, 11, 256, FAKE, None), -3),       # L = 11
+    ((FAKE, FAKE, 5120, 8, 9, 12, 256, FAKE, None), -3),       # k = 9
+    ((FAKE, FAKE, 5120, 8, 0, 12, 256, FAKE, None), -3),       # k = 0
+    ((FAKE, FAKE, 5120, 8, 4, 4, 256, FAKE, None), -3),        # L = k
+    ((FAKE, FAKE, 5120, 8, 8, 7, 256, FAKE, None), -3),        # L < k
+    ((FAKE, FAKE, 5120, 8, 4, 25, 256, FAKE, None), -3),       # L = 25
     ((FAKE, FAKE, 5120, 8, 4, 12, 128, FAKE, None), -3),       # T = 128
     ((FAKE, FAKE, 5000, 8, 4, 12, 256, FAKE, None), -2),       # K % T != 0
     ((FAKE, FAKE, 0, 8, 4, 12, 256, FAKE, None), -2),          # K = 0
@@ -67,7 +70,8 @@ def test_decode_rejects(lib, args, want):
 
 @pytest.mark.parametrize("M,K,N,k,L,T,want", [
     (0, 5120, 64, 4, 12, 256, -3), (-1, 5120, 64, 4, 12, 256, -3), (65537, 5120, 64, 4, 12, 256, -3),
-    (5, 5120, 64, 6, 12, 256, -3), (5, 5000, 64, 4, 12, 256, -2), (5, 5120, 0, 4, 12, 256, -2),
+    (5, 5120, 64, 9, 12, 256, -3), (5, 5120, 64, 2, 2, 256, -3), (5, 5120, 64, 2, 25, 256, -3),
+    (5, 5120, 64, 4, 12, 512, -3), (5, 5000, 64, 4, 12, 256, -2), (5, 5120, 0, 4, 12, 256, -2),
 ])
 def test_gemm_rejects(lib, M, K, N, k, L, T, want):
     assert lib.trellis_gemm(FAKE, FAKE, FAKE, M, K, N, k, L, T, FAKE, None) == want
@@ -77,9 +81,10 @@ def test_gemm_rejects(lib, M, K, N, k, L, T, want):
 
 
 @pytest.mark.parametrize("M", [17, 63, 64, 65, 128, 1000, 65536])
-def test_tensor_core_m_needs_no_workspace(lib, M):
+@pytest.mark.parametrize("k,L", [(4, 12), (1, 2), (8, 24), (5, 16)])
+def test_tensor_core_m_needs_no_workspace(lib, M, k, L):
     n = ctypes.c_size_t(123)
-    assert lib.trellis_gemm_workspace_size(M, 5120, 17408, 4, 12, 256, ctypes.byref(n)) == 0
+    assert lib.trellis_gemm_workspace_size(M, 5120, 17408, k, L, 256, ctypes.byref(n)) == 0
     assert n.value == 0
 
 
@@ -88,7 +93,8 @@ def test_m64_checks_pointers(lib):
     assert lib.trellis_gemm(0, FAKE, FAKE, 64, 5120, 64, 4, 12, 256, FAKE, None) == -1
     assert lib.trellis_gemm(FAKE + 2, FAKE, FAKE, 64, 5120, 64, 4, 12, 256, FAKE, None) == -4
     assert lib.trellis_gemm(FAKE, FAKE, FAKE, 64, 5000, 64, 4, 12, 256, FAKE, None) == -2
-    assert lib.trellis_gemm(FAKE, FAKE, FAKE, 64, 5120, 64, 5, 12, 256, FAKE, None) == -3
+    assert lib.trellis_gemm(FAKE, FAKE, FAKE, 64, 5120, 64, 9, 12, 256, FAKE, None) == -3
+    assert lib.trellis_gemm(FAKE, FAKE, FAKE, 64, 5120, 64, 5, 5, 256, FAKE, None) == -3
 
 
 def test_gemm_rejects_pointers(lib):

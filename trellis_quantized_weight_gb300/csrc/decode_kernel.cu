@@ -24,10 +24,12 @@ namespace trellis {
 constexpr int kDecodeWarps = 8;
 constexpr int kDecodeStageBytes = 4 * kT * 2;   // 4 items of bf16 = 2 KB per warp and buffer
 
-template <int KB>
+// LL: window width fixed at compile time (12), or 0 for the run-time width
+// given by lmask = 2^L - 1.
+template <int KB, int LL>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
-              uint32_t items, FastDiv blocks_per_row, uint16_t* __restrict__ out) {
+              uint32_t items, FastDiv blocks_per_row, uint32_t lmask, uint16_t* __restrict__ out) {
     constexpr int WPB = kGroupsPerBlock * KB;
     __shared__ __align__(128) unsigned char stage[kDecodeWarps][2][kDecodeStageBytes];
 
@@ -42,17 +44,7 @@ decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ s
     auto load = [&](uint32_t base, uint32_t (&w)[KB], float& s) {
         const uint32_t item = base + sub;
         if (item < items) {
-            const uint32_t* p = codes + static_cast<size_t>(item) * WPB + (kGroupsPerBlock - 1 - g) * KB;
-            if constexpr (KB == 4) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-            } else if constexpr (KB == 2) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-                w[0] = v.x; w[1] = v.y;
-            } else {
-#pragma unroll
-                for (int i = 0; i < KB; ++i) w[i] = __ldg(p + i);
-            }
+            ldg_group<KB>(codes + static_cast<size_t>(item) * WPB + (kGroupsPerBlock - 1 - g) * KB, w);
             s = bf16_bits_to_f32(__ldg(scales + blocks_per_row.div(item)));
         } else {
 #pragma unroll
@@ -89,7 +81,8 @@ decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ s
         uint32_t packed[16];
 #pragma unroll
         for (int jp = 0; jp < 16; ++jp) {
-            const float2 v = __fmul2_rn(window_value2(group_window<KB>(w, 2 * jp), group_window<KB>(w, 2 * jp + 1)),
+            const float2 v = __fmul2_rn(window_value2(group_window<KB, LL>(w, 2 * jp, lmask),
+                                                      group_window<KB, LL>(w, 2 * jp + 1, lmask)),
                                         make_float2(cs, cs));
             packed[jp] = pack_bf16x2(v.x, v.y);
         }
@@ -124,7 +117,19 @@ decode_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ s
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
+namespace {
+
+template <int KB, int LL>
+cudaError_t launch_decode_instance(unsigned grid, cudaStream_t stream, const uint32_t* codes,
+                                   const uint16_t* scales, uint32_t items, FastDiv fd, uint32_t lmask,
+                                   uint16_t* out) {
+    return launch_programmatic(decode_kernel<KB, LL>, grid, kDecodeWarps * 32, 0, stream, codes, scales, items, fd,
+                               lmask, out);
+}
+
+}  // namespace
+
+int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k, int L,
                   uint16_t* out, cudaStream_t stream, const DeviceInfo& dev) {
     const uint32_t blocks_per_row = static_cast<uint32_t>(K / kT);
     const uint64_t items64 = static_cast<uint64_t>(N) * blocks_per_row;
@@ -132,14 +137,28 @@ int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, i
     const uint32_t warps_needed = (items + 3u) / 4u;
     const uint32_t ctas_needed = (warps_needed + kDecodeWarps - 1u) / kDecodeWarps;
     const uint32_t max_ctas = static_cast<uint32_t>(dev.num_sms) * 6u;
-    const uint32_t grid = ctas_needed < max_ctas ? ctas_needed : max_ctas;
+    const unsigned grid = ctas_needed < max_ctas ? ctas_needed : max_ctas;
     const FastDiv fd(blocks_per_row);
+    const uint32_t lmask = (1u << L) - 1u;
     cudaError_t e;
-    switch (k) {
-        case 2: e = launch_programmatic(decode_kernel<2>, grid, kDecodeWarps * 32, 0, stream, codes, scales, items, fd, out); break;
-        case 3: e = launch_programmatic(decode_kernel<3>, grid, kDecodeWarps * 32, 0, stream, codes, scales, items, fd, out); break;
-        case 4: e = launch_programmatic(decode_kernel<4>, grid, kDecodeWarps * 32, 0, stream, codes, scales, items, fd, out); break;
-        default: return -3;
+    if (fast_geometry(k, L)) {
+        switch (k) {
+            case 2: e = launch_decode_instance<2, kL>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            case 3: e = launch_decode_instance<3, kL>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            default: e = launch_decode_instance<4, kL>(grid, stream, codes, scales, items, fd, lmask, out); break;
+        }
+    } else {
+        switch (k) {
+            case 1: e = launch_decode_instance<1, 0>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            case 2: e = launch_decode_instance<2, 0>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            case 3: e = launch_decode_instance<3, 0>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            case 4: e = launch_decode_instance<4, 0>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            case 5: e = launch_decode_instance<5, 0>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            case 6: e = launch_decode_instance<6, 0>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            case 7: e = launch_decode_instance<7, 0>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            case 8: e = launch_decode_instance<8, 0>(grid, stream, codes, scales, items, fd, lmask, out); break;
+            default: return -3;
+        }
     }
     return e == cudaSuccess ? 0 : -5;
 }

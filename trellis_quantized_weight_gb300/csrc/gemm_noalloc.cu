@@ -79,10 +79,10 @@ extern "C" int trellis_gemm_noalloc(const uint16_t* x, const uint32_t* codes, co
     int rc = trellis_gemm_workspace_size(M, K, N, k, L, T, &need);   // validates the geometry
     if (rc != TRELLIS_OK) return rc;
     if (need > kNoAllocScratchBytes) return TRELLIS_ERR_WORKSPACE;   // beyond the fixed array
-    if (M > 16) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, out, stream);   // no scratch
+    if (M > 16) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, L, out, stream);   // no scratch
     NoAllocDevice d;
     rc = noalloc_device(d);
     if (rc != TRELLIS_OK) return rc;
-    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, d.scratch, kNoAllocScratchBytes,
+    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, L, out, d.scratch, kNoAllocScratchBytes,
                                        stream, d.info);
 }

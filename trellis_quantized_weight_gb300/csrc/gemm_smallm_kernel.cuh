@@ -72,6 +72,7 @@ struct SmallMPlan {
     uint16_t* out2;
     float* partials;    // workspace: [P][2][WARPS][R*M*4] fp32
     uint32_t* counters; // workspace: [ntg * WARPS]
+    uint32_t lmask;     // 2^L - 1: the window mask of kernels built for a run-time L
 };
 
 // Compile-time shape of one instantiation.
@@ -126,6 +127,11 @@ struct SmallMDefault {
     static constexpr bool ET = MM >= 12;
     using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET>;
     using two = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, true>;   // gate and up
+    // any other (k, L): the quotient table only holds the byte sums that
+    // 12-bit windows reach, so these compute the quotient, which needs more
+    // registers: 8 warps (255 registers a thread) from M = 6 up
+    static constexpr int GWARPS = (MM <= 2) ? 16 : (MM <= 5 ? 12 : 8);
+    using general = SmallMCfg<MM, 3, GWARPS, false, 1, UB, GM, ET>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
 
@@ -194,12 +200,19 @@ __device__ __forceinline__ void load_block_group(const uint32_t* const (&rp)[R],
         if (ok[r]) {
             // volatile: issued where written (a block ahead of its use), never
             // sunk toward the use to shorten register lifetimes
+            // (a group starts at word (7 - g) * KB of a 32-byte aligned block:
+            // 16-byte aligned for KB % 4 == 0, 8-byte aligned for even KB)
             const uint32_t* p = rp[r] + b * WPB + (kGroupsPerBlock - 1 - g) * KB;
-            if constexpr (KB == 4) {
-                asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(w[r][0]), "=r"(w[r][1]), "=r"(w[r][2]), "=r"(w[r][3]) : "l"(p));
-            } else if constexpr (KB == 2) {
-                asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[r][0]), "=r"(w[r][1]) : "l"(p));
+            if constexpr (KB % 4 == 0) {
+#pragma unroll
+                for (int i = 0; i < KB; i += 4)
+                    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w[r][i]), "=r"(w[r][i + 1]), "=r"(w[r][i + 2]), "=r"(w[r][i + 3])
+                                 : "l"(p + i));
+            } else if constexpr (KB % 2 == 0) {
+#pragma unroll
+                for (int i = 0; i < KB; i += 2)
+                    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[r][i]), "=r"(w[r][i + 1]) : "l"(p + i));
             } else {
 #pragma unroll
                 for (int i = 0; i < KB; ++i) asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[r][i]) : "l"(p + i));
@@ -336,7 +349,9 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
     }
 }
 
-template <class C, int KB>
+// LL: the window width when fixed at compile time (12), or 0 for the run-time
+// width of p.lmask.
+template <class C, int KB, int LL>
 __global__ void __launch_bounds__(C::WARPS * 32, C::OCC)
 gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ codes,
                    const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, SmallMPlan p) {
@@ -557,11 +572,12 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                     for (int r = 0; r < R; ++r) {
                         float2 v;
                         if constexpr (C::LUT) {
-                            v.x = quotient_lookup(group_window<KB>(w[r], 2 * pp), lane_tbl);
-                            v.y = quotient_lookup(group_window<KB>(w[r], 2 * pp + 1), lane_tbl);
+                            static_assert(LL == kL, "the quotient table covers 12-bit windows only");
+                            v.x = quotient_lookup(group_window<KB, LL>(w[r], 2 * pp), lane_tbl);
+                            v.y = quotient_lookup(group_window<KB, LL>(w[r], 2 * pp + 1), lane_tbl);
                         } else {
-                            v.x = window_value(group_window<KB>(w[r], 2 * pp));
-                            v.y = window_value(group_window<KB>(w[r], 2 * pp + 1));
+                            v = window_value2(group_window<KB, LL>(w[r], 2 * pp, p.lmask),
+                                              group_window<KB, LL>(w[r], 2 * pp + 1, p.lmask));
                         }
                         const float2 ws = __fmul2_rn(v, s2[r]);
                         const float2 wv = make_float2(round_bf16_as_f32(ws.x), round_bf16_as_f32(ws.y));
@@ -741,12 +757,15 @@ bool smallm_fits_counters(const SmallMPlan& p) {
     return static_cast<size_t>(p.ntg) * C::WARPS <= kCounterCapacity;
 }
 
-template <class C, int KB>
+template <class C, int KB, int LL = kL>
 int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales,
                            int K, int N, uint16_t* out, void* ws, size_t ws_bytes,
-                           cudaStream_t stream, const DeviceInfo& dev, const SecondMatrix& second = SecondMatrix{}) {
+                           cudaStream_t stream, const DeviceInfo& dev, const SecondMatrix& second = SecondMatrix{},
+                           int L = kL) {
     if ((second.codes != nullptr) != C::TWO) return -3;
+    if (LL != 0 && L != LL) return -3;
     SmallMPlan p = plan_smallm<C>(K, N, KB, dev, C::TWO);
+    p.lmask = (1u << L) - 1u;
     p.codes2 = second.codes;
     p.scales2 = second.scales;
     p.out2 = second.out;
@@ -759,12 +778,12 @@ int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint1
     const size_t smem = C::SMEM_BYTES;
     static bool attr_set = false;   // idempotent; a race only repeats the call
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_smallm_kernel<C, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm_smallm_kernel<C, KB, LL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(C::SMEM_BYTES)) != cudaSuccess)
             return -5;
         attr_set = true;
     }
-    const cudaError_t e = launch_programmatic(gemm_smallm_kernel<C, KB>, static_cast<unsigned>(p.P),
+    const cudaError_t e = launch_programmatic(gemm_smallm_kernel<C, KB, LL>, static_cast<unsigned>(p.P),
                                               static_cast<unsigned>(C::WARPS * 32), smem, stream,
                                               x, codes, scales, out, p);
     return e == cudaSuccess ? 0 : -5;
@@ -774,6 +793,13 @@ template <int KB>
 int launch_smallm_k(int M, const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K,
                     int N, uint16_t* out, void* ws, size_t ws_bytes, cudaStream_t stream,
                     const DeviceInfo& dev);
+
+// Any other geometry: k = KB bits, run-time window width L (instantiated in
+// gemm_smallm_g_k*.cu, one translation unit per bit width).
+template <int KB>
+int launch_smallm_g_k(int M, int L, const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int K,
+                      int N, uint16_t* out, void* ws, size_t ws_bytes, cudaStream_t stream,
+                      const DeviceInfo& dev);
 
 // The same with a second matrix sharing x (instantiated in gemm_smallm2_k*.cu).
 template <int KB>

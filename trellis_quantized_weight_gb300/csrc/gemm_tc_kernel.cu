@@ -158,24 +158,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  :: "r"(bar) : "memory");
 }
 
+// Group 4*(stage%2) + gi of block stage/2 of a row, and its lookahead word
+// (only the gi == 0 lanes need one from memory: groups 0 and 4 take it from
+// the other half block, the others from the neighbouring lane).
 template <int KB>
 __device__ __forceinline__ void tc_load_group(const uint32_t* __restrict__ row_codes, bool ok, int stage,
                                               int gi, uint32_t (&w)[KB], uint32_t& extra) {
     constexpr int WPB = kGroupsPerBlock * KB;
     const int b = stage >> 1, g = 4 * (stage & 1) + gi;
     if (ok) {
-        const uint32_t* p = row_codes + b * WPB + (kGroupsPerBlock - 1 - g) * KB;
-        if constexpr (KB == 4) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-        } else if constexpr (KB == 2) {
-            const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-            w[0] = v.x; w[1] = v.y;
-        } else {
-#pragma unroll
-            for (int i = 0; i < KB; ++i) w[i] = __ldg(p + i);
-        }
-        // groups 0 and 4 take their lookahead word from the other half block
+        ldg_group<KB>(row_codes + b * WPB + (kGroupsPerBlock - 1 - g) * KB, w);
         extra = (gi == 0) ? __ldg(row_codes + b * WPB + ((kGroupsPerBlock - g) * KB) % WPB) : 0u;
     } else {
 #pragma unroll
@@ -184,10 +176,12 @@ __device__ __forceinline__ void tc_load_group(const uint32_t* __restrict__ row_c
     }
 }
 
-template <int KB, int NB>
+// LL: window width fixed at compile time (12), or 0 for the run-time width
+// given by lmask = 2^L - 1.
+template <int KB, int NB, int LL>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
-               uint16_t* __restrict__ out, int M, int K, int N, int row_words,
+               uint16_t* __restrict__ out, int M, int K, int N, int row_words, uint32_t lmask,
                const __grid_constant__ CUtensorMap x_map) {
     using S = TcShape<NB>;
     constexpr int kTcStages = S::kStages;
@@ -276,7 +270,8 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                 uint32_t packed[16];
 #pragma unroll
                 for (int jp = 0; jp < 16; ++jp) {
-                    const float2 v = window_value2(group_window<KB>(w, 2 * jp), group_window<KB>(w, 2 * jp + 1));
+                    const float2 v = window_value2(group_window<KB, LL>(w, 2 * jp, lmask),
+                                                   group_window<KB, LL>(w, 2 * jp + 1, lmask));
                     const float2 ws = __fmul2_rn(v, s2);
                     packed[jp] = pack_bf16x2(ws.x, ws.y);
                 }
@@ -408,12 +403,12 @@ bool make_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KB, int NB>
+template <int KB, int NB, int LL>
 int launch_tc_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
-                     uint16_t* out, cudaStream_t stream) {
+                     uint32_t lmask, uint16_t* out, cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<KB, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm_tc_kernel<KB, NB, LL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  TcShape<NB>::kSmemBytes) != cudaSuccess)
             return -5;
         attr_set = true;
@@ -424,10 +419,10 @@ int launch_tc_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* s
         const int mc = (M - m0) < NB ? (M - m0) : NB;
         CUtensorMap map;
         if (!make_x_map(&map, x + static_cast<size_t>(m0) * K, mc, K, tc_box_rows(mc, NB))) return -5;
-        const cudaError_t e = launch_programmatic(gemm_tc_kernel<KB, NB>, static_cast<unsigned>(grid),
+        const cudaError_t e = launch_programmatic(gemm_tc_kernel<KB, NB, LL>, static_cast<unsigned>(grid),
                                                   static_cast<unsigned>(kTcThreads), TcShape<NB>::kSmemBytes,
                                                   stream, codes, scales, out + static_cast<size_t>(m0) * N, mc, K,
-                                                  N, K / 32 * KB, map);
+                                                  N, K / 32 * KB, lmask, map);
         if (e != cudaSuccess) return -5;
     }
     return 0;
@@ -439,22 +434,35 @@ int launch_tc_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* s
 // moved back to end at row M, so it is full and overlaps the one before: the
 // overlapping rows are computed again with identical bits (each output is its
 // own dot product) and written again after the earlier launch (stream order).
-template <int KB>
+template <int KB, int LL>
 int launch_tc_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
-                       uint16_t* out, cudaStream_t stream) {
-    if (M <= 64) return launch_tc_chunks<KB, 64>(x, codes, scales, M, K, N, out, stream);
-    if (M <= 128) return launch_tc_chunks<KB, 128>(x, codes, scales, M, K, N, out, stream);
-    return launch_tc_chunks<KB, 256>(x, codes, scales, M, K, N, out, stream);
+                       int L, uint16_t* out, cudaStream_t stream) {
+    const uint32_t lmask = (1u << L) - 1u;
+    if (M <= 64) return launch_tc_chunks<KB, 64, LL>(x, codes, scales, M, K, N, lmask, out, stream);
+    if (M <= 128) return launch_tc_chunks<KB, 128, LL>(x, codes, scales, M, K, N, lmask, out, stream);
+    return launch_tc_chunks<KB, 256, LL>(x, codes, scales, M, K, N, lmask, out, stream);
 }
 
 }  // namespace
 
 int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N, int k,
-                   uint16_t* out, cudaStream_t stream) {
+                   int L, uint16_t* out, cudaStream_t stream) {
+    if (fast_geometry(k, L)) {
+        switch (k) {
+            case 2: return launch_tc_instance<2, kL>(x, codes, scales, M, K, N, L, out, stream);
+            case 3: return launch_tc_instance<3, kL>(x, codes, scales, M, K, N, L, out, stream);
+            default: return launch_tc_instance<4, kL>(x, codes, scales, M, K, N, L, out, stream);
+        }
+    }
     switch (k) {
-        case 2: return launch_tc_instance<2>(x, codes, scales, M, K, N, out, stream);
-        case 3: return launch_tc_instance<3>(x, codes, scales, M, K, N, out, stream);
-        case 4: return launch_tc_instance<4>(x, codes, scales, M, K, N, out, stream);
+        case 1: return launch_tc_instance<1, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 2: return launch_tc_instance<2, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 3: return launch_tc_instance<3, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 4: return launch_tc_instance<4, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 5: return launch_tc_instance<5, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 6: return launch_tc_instance<6, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 7: return launch_tc_instance<7, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 8: return launch_tc_instance<8, 0>(x, codes, scales, M, K, N, L, out, stream);
         default: return -3;
     }
 }

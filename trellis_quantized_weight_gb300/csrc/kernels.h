@@ -8,10 +8,15 @@
 
 namespace trellis {
 
-// The geometry the kernels are compiled for (the envelope of the page's
-// wrapper: 12-bit windows, 256-weight blocks).
-constexpr int kL_abi = 12;
+// Accepted geometry: 256-weight blocks, k = 1..8 bits per weight, windows of
+// k < L <= 24 bits.  The page's wrapper envelope (k in {2,3,4}, L = 12) runs
+// on kernels specialised for it ("fast geometry": a compile-time window width
+// and, for M <= 16, the shared-memory quotient table); every other (k, L)
+// runs on instantiations with a run-time window mask and the computed
+// quotient.
 constexpr int kT_abi = 256;
+constexpr int kMinK = 1, kMaxK = 8, kMaxL = 24;
+inline bool fast_geometry(int k, int L) { return L == 12 && k >= 2 && k <= 4; }
 
 struct DeviceInfo {
     int device = 0;
@@ -41,7 +46,7 @@ cudaError_t launch_programmatic(void (*kernel)(Params...), unsigned grid, unsign
 }
 
 // Dense decode of all N rows into out [N, K].  Returns 0 or a trellis_status.
-int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k,
+int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k, int L,
                   uint16_t* out, cudaStream_t stream, const DeviceInfo& dev);
 
 // A second weight matrix [N, K] sharing x with the first (gate and up
@@ -52,10 +57,12 @@ struct SecondMatrix {
     uint16_t* out = nullptr;
 };
 
-// Fused decode-and-multiply for 1 <= M <= 16 (CUDA cores).
-size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, const DeviceInfo& dev, bool two = false);
+// Fused decode-and-multiply for 1 <= M <= 16 (CUDA cores).  Both matrices
+// of a SecondMatrix share one launch only for the fast geometry; otherwise
+// the caller runs two launches.
+size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, int L, const DeviceInfo& dev, bool two = false);
 int launch_gemm_smallm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M,
-                       int K, int N, int k, uint16_t* out, void* workspace, size_t workspace_bytes,
+                       int K, int N, int k, int L, uint16_t* out, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream, const DeviceInfo& dev, const SecondMatrix& second = SecondMatrix{});
 
 // act[i] = bf16(silu(g[i]) * u[i]) for count bf16 elements (silu(v) = v / (1 + e^-v),
@@ -63,10 +70,10 @@ int launch_gemm_smallm(const uint16_t* x, const uint32_t* codes, const uint16_t*
 int launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* act, size_t count, cudaStream_t stream,
                     const DeviceInfo& dev);
 
-// Fused decode-and-multiply for M > 16 on the tensor cores (tcgen05), in
-// chunks of 64 activation rows.
+// Fused decode-and-multiply for M > 16 on the tensor cores (tcgen05): one
+// launch per up to 256 activation rows.
 int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N, int k,
-                   uint16_t* out, cudaStream_t stream);
+                   int L, uint16_t* out, cudaStream_t stream);
 // Reads and clears the tensor-core kernel's device error word (bit 0: a
 // bounded wait gave up).  Returns 0 or a trellis_status.
 int tc_take_device_error(unsigned int* flags);

@@ -37,11 +37,13 @@ int device_info(DeviceInfo& out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Checks shared by every entry point (geometry envelope of the page's wrapper:
-// k in {2,3,4}, L = 12, T = 256; K a multiple of T; no fixed K or N).
+// Checks shared by every entry point: T = 256, 1 <= k <= 8, k < L <= 24 (the
+// page's wrapper accepts k in {2,3,4} with L = 12; the same definition holds
+// for the wider set, whose windows still span at most two words); K a
+// multiple of T; no fixed K or N.
 int check_geometry(int K, int N, int k, int L, int T) {
-    if (k != 2 && k != 3 && k != 4) return TRELLIS_ERR_UNSUPPORTED;
-    if (L != trellis::kL_abi || T != trellis::kT_abi) return TRELLIS_ERR_UNSUPPORTED;
+    if (k < trellis::kMinK || k > trellis::kMaxK) return TRELLIS_ERR_UNSUPPORTED;
+    if (L <= k || L > trellis::kMaxL || T != trellis::kT_abi) return TRELLIS_ERR_UNSUPPORTED;
     if (K <= 0 || N <= 0 || K % T != 0) return TRELLIS_ERR_SHAPE;
     // item (row, block) indices and weight offsets must fit the kernels' integer types
     const long long items = static_cast<long long>(N) * (K / T);
@@ -136,7 +138,7 @@ int trellis_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, 
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
-    return trellis::launch_decode(codes, scales, K, N, k, out_bf16, stream, dev);
+    return trellis::launch_decode(codes, scales, K, N, k, L, out_bf16, stream, dev);
 }
 
 int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t* bytes) {
@@ -151,7 +153,7 @@ int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
-    *bytes = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
+    *bytes = trellis::gemm_smallm_workspace_bytes(M, K, N, k, L, dev);
     return *bytes == 0 ? TRELLIS_ERR_SHAPE : TRELLIS_OK;
 }
 
@@ -160,15 +162,15 @@ int trellis_gemm_ws(const uint16_t* x, const uint32_t* codes, const uint16_t* sc
                     cudaStream_t stream) {
     int rc = check_gemm(x, codes, scales, M, K, N, k, L, T, out);
     if (rc != TRELLIS_OK) return rc;
-    if (gemm_on_tensor_cores(M)) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, out, stream);
+    if (gemm_on_tensor_cores(M)) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, L, out, stream);
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
-    const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
+    const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, L, dev);
     if (need == 0) return TRELLIS_ERR_SHAPE;
     if (workspace == nullptr || workspace_bytes < need) return TRELLIS_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return TRELLIS_ERR_ALIGN;
-    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, workspace, workspace_bytes,
+    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, L, out, workspace, workspace_bytes,
                                        stream, dev);
 }
 
@@ -176,16 +178,16 @@ int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scale
                  int k, int L, int T, uint16_t* out, cudaStream_t stream) {
     int rc = check_gemm(x, codes, scales, M, K, N, k, L, T, out);
     if (rc != TRELLIS_OK) return rc;
-    if (gemm_on_tensor_cores(M)) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, out, stream);
+    if (gemm_on_tensor_cores(M)) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, L, out, stream);
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
-    const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev);
+    const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, L, dev);
     if (need == 0) return TRELLIS_ERR_SHAPE;
     void* ws = nullptr;
     rc = owned_workspace(dev, need, &ws);
     if (rc != TRELLIS_OK) return rc;
-    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, out, ws, need, stream, dev);
+    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, L, out, ws, need, stream, dev);
 }
 
 int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T, size_t* bytes) {
@@ -202,7 +204,7 @@ int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T,
     DeviceInfo dev;
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
-    *bytes = trellis::gemm_smallm_workspace_bytes(M, K, N, k, dev, true);
+    *bytes = trellis::gemm_smallm_workspace_bytes(M, K, N, k, L, dev, true);
     return *bytes == 0 ? TRELLIS_ERR_SHAPE : TRELLIS_OK;
 }
 
@@ -222,8 +224,8 @@ int trellis_gemm_gateup(const uint16_t* x, const uint32_t* codes_gate, const uin
     rc = device_info(dev);
     if (rc != TRELLIS_OK) return rc;
     if (gemm_on_tensor_cores(M)) {
-        rc = trellis::launch_gemm_tc(x, codes_gate, scales_gate, M, K, N, k, out_gate, stream);
-        if (rc == TRELLIS_OK) rc = trellis::launch_gemm_tc(x, codes_up, scales_up, M, K, N, k, out_up, stream);
+        rc = trellis::launch_gemm_tc(x, codes_gate, scales_gate, M, K, N, k, L, out_gate, stream);
+        if (rc == TRELLIS_OK) rc = trellis::launch_gemm_tc(x, codes_up, scales_up, M, K, N, k, L, out_up, stream);
     } else {
         if (workspace == nullptr || workspace_bytes < need) return TRELLIS_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return TRELLIS_ERR_ALIGN;
@@ -231,7 +233,7 @@ int trellis_gemm_gateup(const uint16_t* x, const uint32_t* codes_gate, const uin
         up.codes = codes_up;
         up.scales = scales_up;
         up.out = out_up;
-        rc = trellis::launch_gemm_smallm(x, codes_gate, scales_gate, M, K, N, k, out_gate, workspace,
+        rc = trellis::launch_gemm_smallm(x, codes_gate, scales_gate, M, K, N, k, L, out_gate, workspace,
                                          workspace_bytes, stream, dev, up);
     }
     if (rc == TRELLIS_OK && out_act != nullptr)

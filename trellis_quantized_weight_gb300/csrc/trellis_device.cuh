@@ -35,18 +35,50 @@ constexpr uint32_t kMagicBits = 0x4B400000u;
 constexpr float kMagicPlusBias = 12583422.0f;
 
 // Window of weight j (0..31) of a group, from the group's k words w[0..k-1]
-// and the lookahead word w[k].
-template <int KB>
-__device__ __forceinline__ uint32_t group_window(const uint32_t (&w)[KB + 1], int j) {
+// and the lookahead word w[k].  LL is the window width when it is fixed at
+// compile time (the page's L = 12: a window inside one word needs only a
+// shift); LL = 0 takes the width from `lmask` = 2^L - 1 at run time and always
+// funnel-shifts (the same one instruction).  Any 1 <= k <= 8 and L <= 24 keep a
+// window inside words wi and wi + 1 <= k.
+template <int KB, int LL = kL>
+__device__ __forceinline__ uint32_t group_window(const uint32_t (&w)[KB + 1], int j, uint32_t lmask = 0u) {
     const int o = (31 - j) * KB;     // constant after unrolling
     const int wi = o >> 5;
     const int off = o & 31;
-    uint32_t win;
-    if (off + kL <= 32)
-        win = w[wi] >> off;
-    else
-        win = __funnelshift_r(w[wi], w[wi + 1], off);
-    return win & ((1u << kL) - 1u);
+    if constexpr (LL == 0) {
+        return __funnelshift_r(w[wi], w[wi + 1], off) & lmask;
+    } else {
+        uint32_t win;
+        if (off + LL <= 32)
+            win = w[wi] >> off;
+        else
+            win = __funnelshift_r(w[wi], w[wi + 1], off);
+        return win & ((1u << LL) - 1u);
+    }
+}
+
+// The KB code words of one group, starting at p, with the widest loads its
+// alignment allows: a group starts at word (7 - g) * KB of a block and blocks
+// and rows start on 32-byte boundaries, so p is 16-byte aligned when KB is a
+// multiple of 4 and 8-byte aligned when KB is even.
+template <int KB>
+__device__ __forceinline__ void ldg_group(const uint32_t* __restrict__ p, uint32_t (&w)[KB]) {
+    if constexpr (KB % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < KB / 4; ++i) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + i);
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+    } else if constexpr (KB % 2 == 0) {
+#pragma unroll
+        for (int i = 0; i < KB / 2; ++i) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(p) + i);
+            w[2 * i] = v.x; w[2 * i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < KB; ++i) w[i] = __ldg(p + i);
+    }
 }
 
 // float(code) -> code / 147.800537109375 rounded to nearest fp32, as a
@@ -152,26 +184,6 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float f) {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
-}
-
-// Loads the k words of group g of a block (bw = first word of the block) and
-// the lookahead word.
-template <int KB>
-__device__ __forceinline__ void load_group_words(const uint32_t* __restrict__ bw, int g,
-                                                 uint32_t (&w)[KB + 1]) {
-    const uint32_t* p = bw + (kGroupsPerBlock - 1 - g) * KB;
-    if constexpr (KB == 4) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-    } else if constexpr (KB == 2) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-        w[0] = v.x; w[1] = v.y;
-    } else {
-#pragma unroll
-        for (int i = 0; i < KB; ++i) w[i] = __ldg(p + i);
-    }
-    const int la = ((kGroupsPerBlock - g) * KB) % (kGroupsPerBlock * KB);
-    w[KB] = __ldg(bw + la);
 }
 
 // Exact unsigned 32-bit division by a runtime constant d >= 1
