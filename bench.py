@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--entry gemm|decode|gateup] [--rows M]
+                    [--bits k] [--window L]
 
 One step = one fused decode-and-multiply call (trellis_gemm: code fetch,
 window, hash, quotient, scale/bf16 round, M-row FMA, reduction and bf16 store)
@@ -195,7 +196,7 @@ def oracle_throughput(wl, x, codes, scales, budget_s: float, threads: int, max_r
     chunk = max(1, min(rows_total, 64))
 
     def work(r):
-        w = o.decode(codes, scales, wl.K, wl.N, wl.k, rows=r)
+        w = o.decode(codes, scales, wl.K, wl.N, wl.k, L=wl.L, rows=r)
         o.gemm_dense(x, w)
         return r[1] - r[0]
 
@@ -249,7 +250,7 @@ def run_ours(args, wl):
         dcodes_u = [to_dev(codes_u, torch, "u32") for _ in range(n_rot)]
         dscales_u = to_dev(scales_u, torch, "bf16")
         outs = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
-        ws_bytes = binding.gemm_gateup_workspace_bytes(wl.M, wl.K, wl.N, wl.k)
+        ws_bytes = binding.gemm_gateup_workspace_bytes(wl.M, wl.K, wl.N, wl.k, wl.L)
         ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
 
         def call(i):
@@ -261,7 +262,7 @@ def run_ours(args, wl):
                 raise RuntimeError(f"trellis_gemm_gateup failed: {binding.status_string(rc)}")
     elif args.entry == "gemm":
         out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
-        ws_bytes = binding.gemm_workspace_bytes(wl.M, wl.K, wl.N, wl.k)
+        ws_bytes = binding.gemm_workspace_bytes(wl.M, wl.K, wl.N, wl.k, wl.L)
         ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
 
         def call(i):
@@ -352,14 +353,14 @@ def run_ours(args, wl):
             ds2.copy_(hs, non_blocking=True)
             if args.entry == "gemm":
                 dx2.copy_(hx, non_blocking=True)
-                y = tq_gemm(dx2, dc2, ds2, wl.k)
+                y = tq_gemm(dx2, dc2, ds2, wl.k, L=wl.L)
             elif args.entry == "gateup":
                 dx2.copy_(hx, non_blocking=True)
                 dcu2.copy_(hcu, non_blocking=True)
                 dsu2.copy_(hsu, non_blocking=True)
-                y = tq_gateup(dx2, dc2, ds2, dcu2, dsu2, wl.k)[2]   # the activation
+                y = tq_gateup(dx2, dc2, ds2, dcu2, dsu2, wl.k, L=wl.L)[2]   # the activation
             else:
-                y = tq_decode(dc2, ds2, wl.K, wl.k)
+                y = tq_decode(dc2, ds2, wl.K, wl.k, L=wl.L)
             hout.copy_(y, non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -496,7 +497,7 @@ def run_reference(args, wl):
         parts = [(int(a), int(b)) for a, b in zip(edges[:-1], edges[1:]) if b > a]
 
         def work(r):
-            ww = o.decode(codes, scales, wl.K, wl.N, wl.k, rows=r)
+            ww = o.decode(codes, scales, wl.K, wl.N, wl.k, L=wl.L, rows=r)
             o.gemm_dense(x, ww)
         list(ex.map(work, parts))
         return n1 - n0
@@ -539,6 +540,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds for the reference arm's timed run")
     ap.add_argument("--rows", type=int, default=None,
                     help="activation rows M instead of the workload's own (a prefill sweep of the same weights)")
+    ap.add_argument("--bits", type=int, default=None, help="bits per weight k instead of the workload's own (1..8)")
+    ap.add_argument("--window", type=int, default=None, help="window bits L instead of 12 (k < L <= 24)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -549,6 +552,13 @@ def main(argv=None):
             ap.error("--rows must be in 1..65536")
         kind = "gemv" if args.rows == 1 else ("gemm" if args.rows <= 16 else "prefill")
         wl = dataclasses.replace(wl, M=args.rows, name=f"{kind}_m{args.rows}_k{wl.K}_n{wl.N}_k{wl.k}")
+    if args.bits is not None or args.window is not None:
+        k = wl.k if args.bits is None else args.bits
+        L = wl.L if args.window is None else args.window
+        if not (1 <= k <= 8 and k < L <= 24):
+            ap.error("need 1 <= k <= 8 and k < L <= 24")
+        base = wl.name.rsplit("_k", 1)[0]
+        wl = dataclasses.replace(wl, k=k, L=L, name=f"{base}_k{k}" + ("" if L == 12 else f"_L{L}"))
     if args.impl == "reference":
         run_reference(args, wl)
     else:
