@@ -1,7 +1,7 @@
 """Benchmark of the packed-Trellis decode-and-multiply on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--entry gemm|decode|gateup] [--rows M]
+                    [--workload NAME] [--entry gemm|decode|gateup|packed] [--rows M]
                     [--bits k] [--window L]
 
 One step = one fused decode-and-multiply call (trellis_gemm: code fetch,
@@ -27,6 +27,7 @@ from __future__ import annotations
 import argparse
 import dataclasses
 import concurrent.futures as cf
+import ctypes
 import glob
 import hashlib
 import json
@@ -49,6 +50,7 @@ HEADLINE = "gemm_m8_k5120_n17408_k3"
 METRIC = "trellis GEMM packed-weight GB/s"
 METRIC_DECODE = "trellis decode packed-weight GB/s"
 METRIC_GATEUP = "trellis gate/up GEMM packed-weight GB/s"
+METRIC_PACKED = "trellis token-packed GEMM packed-weight GB/s"
 DECODE_OPS_PER_WEIGHT = 10        # algorithmic integer/fp32 ops per decoded weight
 ALU_LANES_PER_SM = 128            # 4 sub-partitions x 32 lanes, one op per lane per clock
 
@@ -219,6 +221,13 @@ def oracle_throughput(wl, x, codes, scales, budget_s: float, threads: int, max_r
 
 
 # ---------------------------------------------------------------- our arm --
+def group_rows(M: int, groups: int) -> list[int]:
+    """M rows split into `groups` sequences whose sizes differ by at most one."""
+    if not 1 <= groups <= M:
+        raise ValueError("--groups must be in 1..M")
+    return [M // groups + (1 if g < M % groups else 0) for g in range(groups)]
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -260,6 +269,23 @@ def run_ours(args, wl):
                                          outs[2].data_ptr(), ws.data_ptr(), ws.numel(), s_handle)
             if rc != 0:
                 raise RuntimeError(f"trellis_gemm_gateup failed: {binding.status_string(rc)}")
+    elif args.entry == "packed":
+        # the workload's M rows as `groups` sequences (sizes as equal as possible),
+        # gathered, multiplied once and scattered back by trellis_gemm_packed
+        rows = group_rows(wl.M, args.groups)
+        offs = np.cumsum([0] + rows)
+        out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+        xp = (ctypes.c_void_p * len(rows))(*[dx[a:b].data_ptr() for a, b in zip(offs[:-1], offs[1:])])
+        op = (ctypes.c_void_p * len(rows))(*[out[a:b].data_ptr() for a, b in zip(offs[:-1], offs[1:])])
+        rp = (ctypes.c_int * len(rows))(*rows)
+        ws_bytes = binding.gemm_packed_workspace_bytes(rows, wl.K, wl.N, wl.k, wl.L)
+        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+
+        def call(i):
+            rc = lib.trellis_gemm_packed(xp, rp, len(rows), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
+                                         wl.K, wl.N, wl.k, wl.L, wl.T, op, ws.data_ptr(), ws.numel(), s_handle)
+            if rc != 0:
+                raise RuntimeError(f"trellis_gemm_packed failed: {binding.status_string(rc)}")
     elif args.entry == "gemm":
         out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
         ws_bytes = binding.gemm_workspace_bytes(wl.M, wl.K, wl.N, wl.k, wl.L)
@@ -341,6 +367,9 @@ def run_ours(args, wl):
         if args.entry == "decode":
             from trellis_quantized_weight_gb300 import decode as tq_decode
             hout = torch.empty((wl.N, wl.K), dtype=torch.bfloat16).pin_memory()
+        if args.entry == "packed":
+            from trellis_quantized_weight_gb300 import gemm_packed as tq_packed
+            ypk = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
         if args.entry == "gateup":
             from trellis_quantized_weight_gb300 import gemm_gateup as tq_gateup
             hcu = torch.from_numpy(codes_u.view(np.int32)).pin_memory()
@@ -354,6 +383,11 @@ def run_ours(args, wl):
             if args.entry == "gemm":
                 dx2.copy_(hx, non_blocking=True)
                 y = tq_gemm(dx2, dc2, ds2, wl.k, L=wl.L)
+            elif args.entry == "packed":
+                dx2.copy_(hx, non_blocking=True)
+                parts = tq_packed([dx2[a:b] for a, b in zip(offs[:-1], offs[1:])], dc2, ds2, wl.k, L=wl.L,
+                                  outs=[ypk[a:b] for a, b in zip(offs[:-1], offs[1:])])
+                y = ypk
             elif args.entry == "gateup":
                 dx2.copy_(hx, non_blocking=True)
                 dcu2.copy_(hcu, non_blocking=True)
@@ -392,14 +426,14 @@ def run_ours(args, wl):
     t_kernel = kernel_ms * 1e-3
     flops = 0
     tensor_peak = float(peaks.get("bf16_tflops") or 1900.0)
-    if args.entry in ("gemm", "gateup") and wl.M > 16:
+    if args.entry in ("gemm", "gateup", "packed") and wl.M > 16:
         # tensor-core path: the decode runs on the ALUs, the M FMAs per weight
         # are a dense bf16 contraction on the tensor cores
         ops = n_mats * wl.weights * DECODE_OPS_PER_WEIGHT
         flops = n_mats * 2 * wl.M * wl.N * wl.K
         hbm_bytes = n_mats * (wl.code_bytes + wl.M * wl.N * 2) + wl.M * wl.K * 2
         kernel_name = "gemm_tc"
-    elif args.entry in ("gemm", "gateup"):
+    elif args.entry in ("gemm", "gateup", "packed"):
         # gate/up: both matrices in one launch, plus the elementwise activation
         # (read 2 and write 1 bf16 [M, N]; bytes counted, no ALU ops)
         ops = n_mats * wl.weights * (DECODE_OPS_PER_WEIGHT + wl.M)
@@ -454,7 +488,8 @@ def run_ours(args, wl):
     if args.entry == "gateup":
         launches_per_step += 1
     line = {
-        "metric": {"gemm": METRIC, "decode": METRIC_DECODE, "gateup": METRIC_GATEUP}[args.entry],
+        "metric": {"gemm": METRIC, "decode": METRIC_DECODE, "gateup": METRIC_GATEUP,
+                   "packed": METRIC_PACKED}[args.entry],
         "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -462,6 +497,7 @@ def run_ours(args, wl):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "entry": "trellis_" + args.entry, "M": wl.M, "K": wl.K, "N": wl.N,
+                   **({"groups": group_rows(wl.M, args.groups)} if args.entry == "packed" else {}),
                    "k": wl.k, "L": wl.L, "T": wl.T, "parallelism": f"replicas{world}",
                    "l2": f"rotating {n_rot} code copies ({n_rot * wl.code_bytes / 1e6:.0f} MB > 2x L2)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
@@ -531,8 +567,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
-    ap.add_argument("--entry", choices=["gemm", "decode", "gateup"], default="gemm",
-                    help="time the fused product (default), the dense decode, or the gate/up pair with its activation")
+    ap.add_argument("--entry", choices=["gemm", "decode", "gateup", "packed"], default="gemm",
+                    help="time the fused product (default), the dense decode, the gate/up pair with its "
+                         "activation, or the token-packed product of --groups sequences")
+    ap.add_argument("--groups", type=int, default=4, help="sequences the M rows are split into (--entry packed)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -559,6 +597,8 @@ def main(argv=None):
             ap.error("need 1 <= k <= 8 and k < L <= 24")
         base = wl.name.rsplit("_k", 1)[0]
         wl = dataclasses.replace(wl, k=k, L=L, name=f"{base}_k{k}" + ("" if L == 12 else f"_L{L}"))
+    if args.entry == "packed" and not 1 <= args.groups <= wl.M:
+        ap.error("--groups must be in 1..M")
     if args.impl == "reference":
         run_reference(args, wl)
     else:

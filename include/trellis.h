@@ -108,11 +108,11 @@ int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, 
  *   1 <= M <= 65536.
  *
  * For M > 16 the decoded bf16 weight tiles are multiplied on the tensor cores
- * (tcgen05, fp32 accumulation in tensor memory), in chunks of 64 activation
- * rows (one launch per chunk; each chunk decodes the weights again; for M > 64
- * not a multiple of 64 the last chunk overlaps the one before and rewrites
- * those rows with the same bits); that path needs no workspace and its waits
- * are bounded (see trellis_device_status).
+ * (tcgen05, fp32 accumulation in tensor memory): one launch serves up to 256
+ * activation rows; larger M runs in 256-row launches, each decoding the
+ * weights again (when M is not a multiple of 256 the last launch overlaps the
+ * one before and rewrites those rows with the same bits).  That path needs no
+ * workspace and its waits are bounded (see trellis_device_status).
  *
  * The summation order is fixed by the launch geometry, so repeated calls on
  * the same device give identical bits.  The kernel balances work across all
@@ -181,8 +181,10 @@ int trellis_device_status(cudaStream_t stream);
  *   out_gate, out_up: device, bf16 [M, N]; out_act: bf16 [M, N] or NULL.
  *   workspace: as trellis_gemm_ws, sized by trellis_gemm_gateup_workspace_size
  *           (0 bytes for M > 16).
- * For M <= 16 both matrices' rows are decoded in one launch (the activations
- * are staged once); for M > 16 each matrix takes the tensor-core path.
+ * For M <= 16 with k in {2,3,4} and L == 12, both matrices' rows are decoded
+ * in one launch (the activations are staged once); other geometries run two
+ * launches through the one workspace; for M > 16 each matrix takes the
+ * tensor-core path.
  * Errors: as trellis_gemm_ws for either matrix; out_act misaligned ->
  * TRELLIS_ERR_ALIGN.
  */
@@ -219,6 +221,49 @@ int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T,
  */
 int trellis_gemm_noalloc(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
                          int K, int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
+
+/*
+ * trellis_gemm_packed — token packing: several independent groups of
+ * activation rows (sequences) multiplied by the same weights in ONE product,
+ * as `mapPackedTokens` on the page "mlx-bun 0.4.0 -> 0.5.0" (token-groups.ts)
+ * packs the real tokens of several sequences for a tokenwise operation and
+ * restores each group's rows afterwards.  Packing raises the M the product
+ * sees, so the weights are decoded once for all groups instead of once per
+ * group.
+ *
+ *   xs      HOST array of `groups` device pointers; xs[g] is bf16 [rows[g], K],
+ *           16-byte aligned.
+ *   rows    HOST array of `groups` row counts, each >= 1; M = sum(rows) must
+ *           be in 1..65536.
+ *   codes, scales, K, N, k, L, T: as trellis_gemm.
+ *   outs    HOST array of `groups` device pointers; outs[g] is bf16
+ *           [rows[g], N], 2-byte aligned; fully overwritten.
+ *   workspace, workspace_bytes: device, 256-byte aligned, zero-filled before
+ *           its first use, at least trellis_gemm_packed_workspace_size bytes;
+ *           it holds the packed x [M, K], the packed output [M, N] and the
+ *           product's own workspace.
+ *
+ * outs[g] equals rows pos_g .. pos_g + rows[g] - 1 of trellis_gemm on the
+ * concatenation of the xs (pos_g = rows of the groups before g): the groups are
+ * gathered with one device-to-device copy each, multiplied once and scattered
+ * back with one copy each, all on `stream`.  One group is multiplied in place
+ * (no copies), as on the page.
+ * Errors: groups < 1 or a NULL array or pointer -> TRELLIS_ERR_NULL or
+ * TRELLIS_ERR_SHAPE (rows[g] < 1); M outside 1..65536 ->
+ * TRELLIS_ERR_UNSUPPORTED; the rest as trellis_gemm_ws.  All checks run before
+ * anything is enqueued.
+ */
+int trellis_gemm_packed(const uint16_t *const *xs, const int *rows, int groups, const uint32_t *codes,
+                        const uint16_t *scales, int K, int N, int k, int L, int T, uint16_t *const *outs,
+                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * trellis_gemm_packed_workspace_size — bytes of workspace trellis_gemm_packed
+ * needs for these groups on the current device.  Same validation as
+ * trellis_gemm_packed for the sizes.
+ */
+int trellis_gemm_packed_workspace_size(const int *rows, int groups, int K, int N, int k, int L, int T,
+                                       size_t *bytes);
 
 #ifdef __cplusplus
 }

@@ -115,3 +115,52 @@ def test_product_path_has_no_oracle_import():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), f
                 assert "trellis_oracle" not in src and "liboracle" not in src, f
+
+
+def _packed_args(rows, xs=None, outs=None):
+    n = len(rows)
+    r = (ctypes.c_int * max(n, 1))(*rows) if rows is not None else None
+    xp = (ctypes.c_void_p * max(n, 1))(*(xs if xs is not None else [FAKE] * n))
+    op = (ctypes.c_void_p * max(n, 1))(*(outs if outs is not None else [FAKE] * n))
+    return xp, r, op
+
+
+@pytest.mark.parametrize("rows,xs,outs,k,L,want", [
+    ([], None, None, 4, 12, -2),                         # no groups
+    ([3, 0, 2], None, None, 4, 12, -2),                  # an empty group
+    ([3, -1], None, None, 4, 12, -2),                    # a negative row count
+    ([40000, 30000], None, None, 4, 12, -3),             # M = 70000 > 65536
+    ([3, 5], [FAKE, 0], None, 4, 12, -1),                # NULL x of group 1
+    ([3, 5], None, [0, FAKE], 4, 12, -1),                # NULL out of group 0
+    ([3, 5], [FAKE, FAKE + 8], None, 4, 12, -4),         # x of group 1 not 16-B aligned
+    ([3, 5], None, [FAKE, FAKE + 1], 4, 12, -4),         # odd out address
+    ([30, 40], None, None, 9, 12, -3),                   # k = 9
+    ([30, 40], None, None, 4, 4, -3),                    # L = k
+    ([30, 40], None, None, 4, 12, -7),                   # workspace of 256 bytes (needs MiBs)
+])
+def test_packed_rejects(lib, rows, xs, outs, k, L, want):
+    xp, r, op = _packed_args(rows, xs, outs)
+    assert lib.trellis_gemm_packed(xp, r, len(rows), FAKE, FAKE, 5120, 64, k, L, 256, op, FAKE, 256, None) == want
+
+
+def test_packed_rejects_null_arrays(lib):
+    xp, r, op = _packed_args([3, 5])
+    assert lib.trellis_gemm_packed(None, r, 2, FAKE, FAKE, 5120, 64, 4, 12, 256, op, FAKE, 1 << 30, None) == -1
+    assert lib.trellis_gemm_packed(xp, None, 2, FAKE, FAKE, 5120, 64, 4, 12, 256, op, FAKE, 1 << 30, None) == -1
+    assert lib.trellis_gemm_packed(xp, r, 2, FAKE, FAKE, 5120, 64, 4, 12, 256, None, FAKE, 1 << 30, None) == -1
+    assert lib.trellis_gemm_packed(xp, r, 2, 0, FAKE, 5120, 64, 4, 12, 256, op, FAKE, 1 << 30, None) == -1
+
+
+def test_packed_workspace_size_on_the_tensor_core_path(lib):
+    """M > 16 needs no product workspace, but the counter region (1 MiB) stays
+    reserved ahead of the packed x and output."""
+    rows, K, N = [30, 40], 5120, 17408
+    r = (ctypes.c_int * 2)(*rows)
+    n = ctypes.c_size_t(0)
+    assert lib.trellis_gemm_packed_workspace_size(r, 2, K, N, 4, 12, 256, ctypes.byref(n)) == 0
+    r256 = lambda b: (b + 255) // 256 * 256
+    assert n.value == (1 << 20) + r256(70 * K * 2) + r256(70 * N * 2)
+    one = (ctypes.c_int * 1)(70)
+    assert lib.trellis_gemm_packed_workspace_size(one, 1, K, N, 4, 12, 256, ctypes.byref(n)) == 0
+    assert n.value == 0    # one group runs in place on the tensor cores
+    assert lib.trellis_gemm_packed_workspace_size(r, 2, K, N, 4, 12, 256, None) == -1

@@ -5,8 +5,8 @@ behind the C ABI declared in ``include/trellis.h``); this package only builds
 it (``build.build()``), binds it (``binding``) and draws seeded synthetic inputs
 (``synth``).  Calls fail loudly when the library is missing.
 """
-from .binding import (TrellisError, decode, gemm, gemm_gateup, gemm_gateup_workspace_bytes, gemm_workspace_bytes,
-                      load, status_string)
+from .binding import (TrellisError, decode, gemm, gemm_gateup, gemm_gateup_workspace_bytes, gemm_packed,
+                      gemm_packed_workspace_bytes, gemm_workspace_bytes, load, status_string)
 
-__all__ = ["TrellisError", "decode", "gemm", "gemm_gateup", "gemm_gateup_workspace_bytes", "gemm_workspace_bytes",
-           "load", "status_string"]
+__all__ = ["TrellisError", "decode", "gemm", "gemm_gateup", "gemm_gateup_workspace_bytes", "gemm_packed",
+           "gemm_packed_workspace_bytes", "gemm_workspace_bytes", "load", "status_string"]

@@ -36,6 +36,8 @@ SIGNATURES = {
     "trellis_device_status": (_I, [_P]),
     "trellis_gemm_gateup": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "trellis_gemm_gateup_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
+    "trellis_gemm_packed": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "trellis_gemm_packed_workspace_size": (_I, [_P, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
 }
 
 
@@ -105,6 +107,14 @@ def gemm_gateup_workspace_bytes(M, K, N, k, L=12, T=256) -> int:
     n = ctypes.c_size_t(0)
     _check(load().trellis_gemm_gateup_workspace_size(M, K, N, k, L, T, ctypes.byref(n)),
            "trellis_gemm_gateup_workspace_size")
+    return int(n.value)
+
+
+def gemm_packed_workspace_bytes(rows, K, N, k, L=12, T=256) -> int:
+    r = (ctypes.c_int * len(rows))(*rows)
+    n = ctypes.c_size_t(0)
+    _check(load().trellis_gemm_packed_workspace_size(r, len(rows), K, N, k, L, T, ctypes.byref(n)),
+           "trellis_gemm_packed_workspace_size")
     return int(n.value)
 
 
@@ -215,3 +225,36 @@ def gemm_gateup(x, codes_gate, scales_gate, codes_up, scales_up, k: int, act: bo
     _check(rc, "trellis_gemm_gateup")
     return g, u, a
 
+
+
+def gemm_packed(xs, codes, scales, k: int, L: int = 12, T: int = 256, outs=None, stream=None):
+    """Token packing: one product for several groups of activation rows sharing the
+    weights.  xs: list of bf16 [rows_g, K]; returns the list of bf16 [rows_g, N]."""
+    torch = _torch()
+    xs = list(xs)
+    if not xs:
+        raise ValueError("xs must hold at least one group")
+    for i, x in enumerate(xs):
+        _require(x, f"xs[{i}]", (torch.bfloat16,), 2)
+    _require(codes, "codes", (torch.int32, torch.uint32), 2)
+    _require(scales, "scales", (torch.bfloat16,), 1)
+    K = xs[0].shape[1]
+    N = codes.shape[0]
+    if any(x.shape[1] != K for x in xs) or codes.shape[1] * 32 != K * k or scales.numel() != N:
+        raise ValueError("every x must be [rows, K] with codes [N, K*k/32] and scales [N]")
+    rows = [int(x.shape[0]) for x in xs]
+    if outs is None:
+        outs = [torch.empty((r, N), dtype=torch.bfloat16, device=xs[0].device) for r in rows]
+    for i, (o, r) in enumerate(zip(outs, rows)):
+        _require(o, f"outs[{i}]", (torch.bfloat16,), 2)
+        if tuple(o.shape) != (r, N):
+            raise ValueError(f"outs[{i}] must be [{r}, {N}]")
+    nbytes = gemm_packed_workspace_bytes(rows, K, N, k, L, T)
+    ws = _workspace(xs[0].device, max(nbytes, 256))
+    xp = (ctypes.c_void_p * len(xs))(*[x.data_ptr() for x in xs])
+    op = (ctypes.c_void_p * len(outs))(*[o.data_ptr() for o in outs])
+    rp = (ctypes.c_int * len(rows))(*rows)
+    rc = load().trellis_gemm_packed(xp, rp, len(rows), codes.data_ptr(), scales.data_ptr(), K, N, k, L, T, op,
+                                    ws.data_ptr(), ws.numel(), _stream_handle(xs[0].device, stream))
+    _check(rc, "trellis_gemm_packed")
+    return outs
