@@ -487,6 +487,8 @@ def run_ours(args, wl):
     launches_per_step = n_mats * chunks if wl.M > 16 and args.entry != "decode" else 1
     if args.entry == "gateup":
         launches_per_step += 1
+    if args.entry == "packed" and args.groups > 1:   # the gather and the scatter, per 64 groups
+        launches_per_step += 2 * ((args.groups + 63) // 64)
     line = {
         "metric": {"gemm": METRIC, "decode": METRIC_DECODE, "gateup": METRIC_GATEUP,
                    "packed": METRIC_PACKED}[args.entry],

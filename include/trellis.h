@@ -245,9 +245,9 @@ int trellis_gemm_noalloc(const uint16_t *x, const uint32_t *codes, const uint16_
  *
  * outs[g] equals rows pos_g .. pos_g + rows[g] - 1 of trellis_gemm on the
  * concatenation of the xs (pos_g = rows of the groups before g): the groups are
- * gathered with one device-to-device copy each, multiplied once and scattered
- * back with one copy each, all on `stream`.  One group is multiplied in place
- * (no copies), as on the page.
+ * gathered by one copy kernel (per 64 groups), multiplied once and scattered
+ * back by one more, all on `stream`.  One group is multiplied in place (no
+ * copies), as on the page.
  * Errors: groups < 1 or a NULL array or pointer -> TRELLIS_ERR_NULL or
  * TRELLIS_ERR_SHAPE (rows[g] < 1); M outside 1..65536 ->
  * TRELLIS_ERR_UNSUPPORTED; the rest as trellis_gemm_ws.  All checks run before

@@ -1,13 +1,16 @@
 // Token packing (trellis_gemm_packed): several groups of activation rows
 // multiplied by the same weights in one product (mapPackedTokens on the page
-// "mlx-bun 0.4.0 -> 0.5.0", token-groups.ts).  Host code only: the groups are
-// gathered into a packed x with one device-to-device copy each, the product
-// runs once through trellis_gemm_ws, and the packed output rows are copied
-// back to each group's output.
+// "mlx-bun 0.4.0 -> 0.5.0", token-groups.ts): the groups are gathered into a
+// packed x by one copy launch (copy_groups.cu, up to 64 groups a launch), the
+// product runs once through trellis_gemm_ws, and one more copy launch scatters
+// the packed output rows back to each group's output.
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "kernels.h"
 #include "trellis.h"
+
+using trellis::DeviceInfo;
 
 namespace {
 
@@ -95,24 +98,44 @@ int trellis_gemm_packed(const uint16_t* const* xs, const int* rows, int groups, 
         return trellis_gemm_ws(xs[0], codes, scales, static_cast<int>(M), K, N, k, L, T, outs[0], gemm_ws,
                                lay.gemm_bytes, stream);
 
+    DeviceInfo dev;
+    if (cudaGetDevice(&dev.device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&dev.num_sms, cudaDevAttrMultiProcessorCount, dev.device) != cudaSuccess)
+        return TRELLIS_ERR_CUDA;
     uint16_t* px = reinterpret_cast<uint16_t*>(ws + lay.x_off);
     uint16_t* pout = reinterpret_cast<uint16_t*>(ws + lay.out_off);
+    // gather: group g's rows to packed rows pos_g .., kCopyBatch groups a launch
     size_t pos = 0;
-    for (int g = 0; g < groups; ++g) {
-        const size_t n = static_cast<size_t>(rows[g]);
-        if (cudaMemcpyAsync(px + pos * K, xs[g], n * K * 2, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-            return TRELLIS_ERR_CUDA;
-        pos += n;
+    for (int g0 = 0; g0 < groups; g0 += trellis::kCopyBatch) {
+        const int nb = groups - g0 < trellis::kCopyBatch ? groups - g0 : trellis::kCopyBatch;
+        trellis::CopyBatch b;
+        for (int j = 0; j < nb; ++j) {
+            const size_t n = static_cast<size_t>(rows[g0 + j]);
+            b.src[j] = xs[g0 + j];
+            b.dst[j] = px + pos * K;
+            b.count[j] = n * K;
+            pos += n;
+        }
+        rc = trellis::launch_copy_groups(b, nb, stream, dev);
+        if (rc != TRELLIS_OK) return rc;
     }
     rc = trellis_gemm_ws(px, codes, scales, static_cast<int>(M), K, N, k, L, T, pout, gemm_ws, lay.gemm_bytes,
                          stream);
     if (rc != TRELLIS_OK) return rc;
+    // scatter: packed output rows back to each group's output
     pos = 0;
-    for (int g = 0; g < groups; ++g) {
-        const size_t n = static_cast<size_t>(rows[g]);
-        if (cudaMemcpyAsync(outs[g], pout + pos * N, n * N * 2, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-            return TRELLIS_ERR_CUDA;
-        pos += n;
+    for (int g0 = 0; g0 < groups; g0 += trellis::kCopyBatch) {
+        const int nb = groups - g0 < trellis::kCopyBatch ? groups - g0 : trellis::kCopyBatch;
+        trellis::CopyBatch b;
+        for (int j = 0; j < nb; ++j) {
+            const size_t n = static_cast<size_t>(rows[g0 + j]);
+            b.src[j] = pout + pos * N;
+            b.dst[j] = outs[g0 + j];
+            b.count[j] = n * N;
+            pos += n;
+        }
+        rc = trellis::launch_copy_groups(b, nb, stream, dev);
+        if (rc != TRELLIS_OK) return rc;
     }
     return TRELLIS_OK;
 }

@@ -74,6 +74,18 @@ int launch_silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* act, size_t 
 // launch per up to 256 activation rows.
 int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N, int k,
                    int L, uint16_t* out, cudaStream_t stream);
+// Copies of up to kCopyBatch contiguous runs of bf16 elements (count[g]
+// elements from src[g] to dst[g]) in one launch, chained by programmatic
+// launch: the gather and scatter of trellis_gemm_packed.  Returns 0 or a
+// trellis_status.
+constexpr int kCopyBatch = 64;
+struct CopyBatch {
+    const uint16_t* src[kCopyBatch];
+    uint16_t* dst[kCopyBatch];
+    unsigned long long count[kCopyBatch];
+};
+int launch_copy_groups(const CopyBatch& batch, int groups, cudaStream_t stream, const DeviceInfo& dev);
+
 // Reads and clears the tensor-core kernel's device error word (bit 0: a
 // bounded wait gave up).  Returns 0 or a trellis_status.
 int tc_take_device_error(unsigned int* flags);
