@@ -160,10 +160,22 @@ int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *sc
  * trellis_device_status — synchronise `stream`, then report whether a bounded
  * device-side wait of the tensor-core product gave up since the last query
  * (TRELLIS_ERR_TIMEOUT; the affected outputs are undefined) or not
- * (TRELLIS_OK).  Clears the flag.  No counterpart on the pages: it is how the
- * library surfaces its own wait limits.
+ * (TRELLIS_OK).  Clears the flag.  A wait gives up after 2 s of wall-clock
+ * time; the kernel then winds down and returns, so the context stays usable.
+ * No counterpart on the pages: it is how the library surfaces its own wait
+ * limits.
  */
 int trellis_device_status(cudaStream_t stream);
+
+/*
+ * trellis_selftest_wait_timeout — enqueue on `stream` a one-thread kernel
+ * whose bounded wait (50 ms) runs out because nothing arrives on its barrier;
+ * it sets the same device error word as a product wait that gives up, so the
+ * next trellis_device_status returns TRELLIS_ERR_TIMEOUT.  Checks the failure
+ * reporting path without a hang or a fault.  Returns TRELLIS_OK or
+ * TRELLIS_ERR_CUDA.
+ */
+int trellis_selftest_wait_timeout(cudaStream_t stream);
 
 /*
  * trellis_gemm_gateup — the two projections of a gated MLP that share x, in

@@ -359,3 +359,63 @@ def test_full_gemm(tq, oracle_lib, full_inputs, name):
     w = oracle_decode_par(oracle_lib, codes, scales, wl.K, wl.N, wl.k)
     ref, refabs = oracle_gemm_par(oracle_lib, x, w)
     assert_gemm_close(got, ref, refabs, name)
+
+
+def test_gemm_largest_m(tq, oracle_lib):
+    """M = 65536, the largest accepted: 256 tensor-core launches of 256 rows.
+    Checked against the oracle on sampled activation rows (the first and last
+    rows, both sides of several launch boundaries, and random rows), with the
+    rows after the output left untouched."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    M, K, N, k = 65536, 256, 130, 3
+    x, codes, scales = _inputs(M, K, N, k, seed=9901)
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    pad = 2
+    out = torch.full(((M + pad) * N,), 0x7FC1, dtype=torch.int16, device="cuda")
+    ws = torch.zeros(max(binding.gemm_workspace_bytes(M, K, N, k), 256), dtype=torch.uint8, device="cuda")
+    rc = binding.abi_gemm_ws(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256, out.data_ptr(),
+                             ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, binding.status_string(rc)
+    torch.cuda.synchronize()
+    assert binding.load().trellis_device_status(None) == 0
+    bits = out.cpu().numpy().view(np.uint16)
+    assert np.all(bits[M * N:] == 0x7FC1)
+    got = bits[: M * N].reshape(M, N)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 1, 255, 256, 257, 32767, 32768, 65279, 65280, 65535],
+                                     rng.integers(0, M, 100)]))
+    w = oracle_lib.decode(codes, scales, K, N, k)
+    ref, refabs = oracle_lib.gemm_dense(x[rows], w)
+    assert_gemm_close(got[rows], ref, refabs, "M=65536 sampled rows")
+
+
+@pytest.mark.parametrize("M", [8, 64])
+def test_gemm_long_k(tq, oracle_lib, M):
+    """K = 51200 (200 blocks a row, 400 tensor-core stages): long reductions on
+    both paths."""
+    N, K, k = 200, 256 * 200, 2
+    x, codes, scales = _inputs(M, K, N, k, seed=9911 + M)
+    got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), k))
+    w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+    ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+    assert_gemm_close(got, ref, refabs, f"M={M} K={K}")
+
+
+def test_wait_timeout_is_reported_and_the_context_stays_usable(tq, oracle_lib):
+    """A bounded device-side wait that runs out (the self-test kernel waits on a
+    barrier that nothing arrives on) is reported by trellis_device_status as
+    TRELLIS_ERR_TIMEOUT once, the flag clears, and the next product is correct."""
+    from trellis_quantized_weight_gb300 import binding
+    lib = binding.load()
+    assert lib.trellis_device_status(None) == 0
+    assert lib.trellis_selftest_wait_timeout(None) == 0
+    assert lib.trellis_device_status(None) == -6
+    assert lib.trellis_device_status(None) == 0
+    M, K, N, k = 64, 512, 300, 4
+    x, codes, scales = _inputs(M, K, N, k, seed=9950)
+    got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), k))
+    assert lib.trellis_device_status(None) == 0
+    w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+    ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+    assert_gemm_close(got, ref, refabs, "after the self-test")

@@ -34,6 +34,7 @@ SIGNATURES = {
     "trellis_gemm_ws": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "trellis_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "trellis_device_status": (_I, [_P]),
+    "trellis_selftest_wait_timeout": (_I, [_P]),
     "trellis_gemm_gateup": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "trellis_gemm_gateup_workspace_size": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
     "trellis_gemm_packed": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),

@@ -97,7 +97,11 @@ struct TcShape {
                   "swizzle atoms must start on 1 KB boundaries");
 };
 
-constexpr uint32_t kWaitLimit = 1u << 24;   // polls before a wait gives up
+// A wait gives up after kWaitNs of wall-clock time (the %globaltimer
+// nanosecond clock, read every 64 polls) or, as a backstop, after
+// kWaitPollCap polls, whichever comes first.
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
+constexpr uint32_t kWaitPollCap = 1u << 26;
 
 
 
@@ -118,13 +122,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
                  " selp.b32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0u;
 }
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 // Bounded wait: false (and the error word set) when it runs out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 0; i < kWaitPollCap; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && global_ns() - t0 > limit_ns) break;
+    }
     atomicOr(&g_tc_error, 1u);
     return false;
 }
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_for(bar, parity, kWaitNs); }
 __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -465,6 +478,27 @@ int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* sca
         case 8: return launch_tc_instance<8, 0>(x, codes, scales, M, K, N, L, out, stream);
         default: return -3;
     }
+}
+
+namespace {
+
+// One thread waits on an mbarrier that nothing ever arrives on: the wait runs
+// out after limit_ns, sets the error word and the kernel returns.  It checks
+// the reporting path of the product's bounded waits without a hang or fault.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    (void)mbar_wait_for(b, 0, limit_ns);
+}
+
+}  // namespace
+
+int launch_wait_selftest(cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(50000000ull);   // 50 ms
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
 int tc_take_device_error(unsigned int* flags) {

@@ -86,6 +86,10 @@ struct CopyBatch {
 };
 int launch_copy_groups(const CopyBatch& batch, int groups, cudaStream_t stream, const DeviceInfo& dev);
 
+// Launches one thread whose bounded wait on an mbarrier runs out (nothing
+// arrives), which sets the device error word exactly as a product wait that
+// gives up would.  Returns 0 or a trellis_status.
+int launch_wait_selftest(cudaStream_t stream);
 // Reads and clears the tensor-core kernel's device error word (bit 0: a
 // bounded wait gave up).  Returns 0 or a trellis_status.
 int tc_take_device_error(unsigned int* flags);

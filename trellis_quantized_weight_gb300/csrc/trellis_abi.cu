@@ -241,6 +241,8 @@ int trellis_gemm_gateup(const uint16_t* x, const uint32_t* codes_gate, const uin
     return rc;
 }
 
+int trellis_selftest_wait_timeout(cudaStream_t stream) { return trellis::launch_wait_selftest(stream); }
+
 int trellis_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return TRELLIS_ERR_CUDA;
     unsigned int flags = 0u;
