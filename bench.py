@@ -96,11 +96,24 @@ def _code_only(text: str) -> str:
     return "\n".join(line.strip() for line in text.splitlines() if line.strip())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources' code (comments ignored): names the kernels an
-    ncu capture in profiles/ was taken on."""
+# The sources each profiled kernel is built from (plus the shared headers).
+KERNEL_SOURCES = {
+    "decode": ["decode_kernel.cu"],
+    "gemm_smallm": ["gemm_smallm_kernel.cuh", "gemm_smallm.cu", "gemm_smallm_k*.cu"],
+    "gemm_tc": ["gemm_tc_kernel.cu"],
+}
+SHARED_SOURCES = ["trellis_device.cuh", "kernels.h"]
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the code (comments ignored) of one kernel's sources and the
+    shared headers: names the kernel an ncu capture in profiles/ was taken on."""
+    csrc = os.path.join(ROOT, "trellis_quantized_weight_gb300", "csrc")
+    files = set()
+    for pat in KERNEL_SOURCES[kernel] + SHARED_SOURCES:
+        files.update(glob.glob(os.path.join(csrc, pat)))
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "trellis_quantized_weight_gb300", "csrc", "*"))):
+    for f in sorted(files):
         with open(f, encoding="utf-8") as fh:
             h.update(os.path.basename(f).encode())
             h.update(_code_only(fh.read()).encode())
@@ -119,7 +132,7 @@ def profiled_traffic(kernel: str, workload: str):
             if line.startswith("- ") and ":" in line:
                 key, val = line[2:].split(":", 1)
                 vals[key.strip()] = val.strip().strip("`")
-    if vals.get("kernel_source_hash") != kernel_source_hash():
+    if vals.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     try:
         return int(float(vals["dram_bytes_per_launch"]))
