@@ -102,7 +102,7 @@ KERNEL_SOURCES = {
     "gemm_smallm": ["gemm_smallm_kernel.cuh", "gemm_smallm.cu", "gemm_smallm_k*.cu"],
     "gemm_tc": ["gemm_tc_kernel.cu"],
 }
-SHARED_SOURCES = ["trellis_device.cuh", "kernels.h"]
+SHARED_SOURCES = ["trellis_device.cuh"]   # device code shared by all kernels (kernels.h is host plumbing)
 
 
 def kernel_source_hash(kernel: str) -> str:

@@ -776,13 +776,8 @@ int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint1
     p.counters = static_cast<uint32_t*>(ws);
     p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
     const size_t smem = C::SMEM_BYTES;
-    static bool attr_set = false;   // idempotent; a race only repeats the call
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_smallm_kernel<C, KB, LL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(C::SMEM_BYTES)) != cudaSuccess)
-            return -5;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> opted{0};
+    if (!smem_opt_in(gemm_smallm_kernel<C, KB, LL>, static_cast<int>(C::SMEM_BYTES), opted)) return -5;
     const cudaError_t e = launch_programmatic(gemm_smallm_kernel<C, KB, LL>, static_cast<unsigned>(p.P),
                                               static_cast<unsigned>(C::WARPS * 32), smem, stream,
                                               x, codes, scales, out, p);

@@ -419,13 +419,8 @@ bool make_x_map(CUtensorMap* map, const uint16_t* x, int M, int K, int rows) {
 template <int KB, int NB, int LL>
 int launch_tc_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
                      uint32_t lmask, uint16_t* out, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<KB, NB, LL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcShape<NB>::kSmemBytes) != cudaSuccess)
-            return -5;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> opted{0};
+    if (!smem_opt_in(gemm_tc_kernel<KB, NB, LL>, TcShape<NB>::kSmemBytes, opted)) return -5;
     const int grid = (N + kTcRows - 1) / kTcRows;
     for (int m = 0; m < M; m += NB) {
         const int m0 = (M > NB && m + NB > M) ? M - NB : m;

@@ -2,6 +2,7 @@
 // translation units.  Arguments reaching these functions are already validated.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -23,6 +24,22 @@ struct DeviceInfo {
     int num_sms = 0;
     int max_smem_optin = 0;   // bytes of dynamic shared memory a CTA may opt into
 };
+
+// Opts `kernel` into `bytes` of dynamic shared memory on the current device.
+// The attribute belongs to the device, so each call site keeps one bit per
+// device (`done`) and calls cudaFuncSetAttribute once per device; a race only
+// repeats the call.  Returns false on a CUDA error.
+template <class Kernel>
+bool smem_opt_in(Kernel kernel, int bytes, std::atomic<unsigned long long>& done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return false;
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return true;
+}
 
 // Launch with programmatic stream serialization: the grid may begin while the
 // previous kernel on the stream is still draining.  Kernels launched this way
