@@ -65,7 +65,7 @@ def test_decode_crafted_blocks(tq, oracle_lib, k):
 
 # -------------------------------------------------------------------- gemm --
 @pytest.mark.parametrize("k", [2, 3, 4])
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 12, 15, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16])
 def test_gemm_small(tq, oracle_lib, M, k):
     N, K = 1000, 1024
     x, codes, scales = _inputs(M, K, N, k, seed=77 * M + k)

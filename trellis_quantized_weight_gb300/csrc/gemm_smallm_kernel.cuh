@@ -118,10 +118,12 @@ struct SmallMCfg {
 
 // The shape used by the library for each M, chosen by timing back-to-back
 // calls of the M = 1, 5, 8 and 15 workloads on GB300 over R, WARPS, UB, LUT and
-// CTAs per SM (M in between takes its neighbours' shape).
+// CTAs per SM (M in between takes its neighbours' shape).  M = 11 takes 8 warps:
+// at 12 warps its registers (168 a thread) spill, and 8 warps measured 7-12%
+// faster; M = 9 and 10 measured the same or faster at 12.
 template <int MM>
 struct SmallMDefault {
-    static constexpr int WARPS = (MM <= 2) ? 16 : (MM <= 11 ? 12 : 8);
+    static constexpr int WARPS = (MM <= 2) ? 16 : (MM <= 10 ? 12 : 8);
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
     static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
     static constexpr bool ET = MM >= 12;
