@@ -365,6 +365,10 @@ def run_ours(args, wl):
     ms_step, kernel_ms, isolated_ms = max_over_ranks([ms_step, kernel_ms, isolated_ms], device="cuda")
 
     # ---- end to end through the public API, host buffers in pinned memory ----
+    # Every step uploads its inputs from pinned host memory and reads its result
+    # back.  Two device buffer sets let step i+1's uploads (two copy streams,
+    # each carrying half of the codes) run while step i's product runs; a set is
+    # overwritten only after the product that read it has finished.
     e2e = None
     if not args.no_e2e:
         from trellis_quantized_weight_gb300 import gemm as tq_gemm
@@ -372,11 +376,8 @@ def run_ours(args, wl):
         hc = torch.from_numpy(codes.view(np.int32)).pin_memory()
         hs = torch.from_numpy(scales.view(np.int16)).view(torch.bfloat16).pin_memory()
         hout = torch.empty((wl.M, wl.N), dtype=torch.bfloat16).pin_memory()
-        dx2 = torch.empty_like(dx)
-        dc2 = torch.empty_like(dcodes[0])
-        ds2 = torch.empty_like(dscales)
         n_e2e = max(3, min(args.steps, args.e2e_steps))
-
+        hcu = hsu = None
         if args.entry == "decode":
             from trellis_quantized_weight_gb300 import decode as tq_decode
             hout = torch.empty((wl.N, wl.K), dtype=torch.bfloat16).pin_memory()
@@ -387,49 +388,85 @@ def run_ours(args, wl):
             from trellis_quantized_weight_gb300 import gemm_gateup as tq_gateup
             hcu = torch.from_numpy(codes_u.view(np.int32)).pin_memory()
             hsu = torch.from_numpy(scales_u.view(np.int16)).view(torch.bfloat16).pin_memory()
-            dcu2 = torch.empty_like(dcodes_u[0])
-            dsu2 = torch.empty_like(dscales_u)
+        bufs = []
+        for _ in range(2):
+            b = {"x": torch.empty_like(dx), "c": torch.empty_like(dcodes[0]), "s": torch.empty_like(dscales)}
+            if hcu is not None:
+                b["cu"] = torch.empty_like(dcodes[0])
+                b["su"] = torch.empty_like(dscales)
+            bufs.append(b)
+        copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        free = [None, None]            # event: the product that read set b has finished
+        half = hc.shape[0] // 2
 
-        def e2e_step():
-            dc2.copy_(hc, non_blocking=True)
-            ds2.copy_(hs, non_blocking=True)
-            if args.entry == "gemm":
-                dx2.copy_(hx, non_blocking=True)
-                y = tq_gemm(dx2, dc2, ds2, wl.k, L=wl.L)
-            elif args.entry == "packed":
-                dx2.copy_(hx, non_blocking=True)
-                parts = tq_packed([dx2[a:b] for a, b in zip(offs[:-1], offs[1:])], dc2, ds2, wl.k, L=wl.L,
-                                  outs=[ypk[a:b] for a, b in zip(offs[:-1], offs[1:])])
-                y = ypk
-            elif args.entry == "gateup":
-                dx2.copy_(hx, non_blocking=True)
-                dcu2.copy_(hcu, non_blocking=True)
-                dsu2.copy_(hsu, non_blocking=True)
-                y = tq_gateup(dx2, dc2, ds2, dcu2, dsu2, wl.k, L=wl.L)[2]   # the activation
-            else:
-                y = tq_decode(dc2, ds2, wl.K, wl.k, L=wl.L)
-            hout.copy_(y, non_blocking=True)
+        def upload(bi, after=None):
+            b = bufs[bi]
+            done = []
+            for j, cs in enumerate(copy_streams):
+                if free[bi] is not None:
+                    cs.wait_event(free[bi])
+                if after is not None:
+                    cs.wait_event(after)
+                rows = slice(0, half) if j == 0 else slice(half, None)
+                with torch.cuda.stream(cs):
+                    b["c"][rows].copy_(hc[rows], non_blocking=True)
+                    if hcu is not None:
+                        b["cu"][rows].copy_(hcu[rows], non_blocking=True)
+                    if j == 1:
+                        b["s"].copy_(hs, non_blocking=True)
+                        if hsu is not None:
+                            b["su"].copy_(hsu, non_blocking=True)
+                        if args.entry != "decode":
+                            b["x"].copy_(hx, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(cs)
+                    done.append(ev)
+            return done
 
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                e2e_step()
+        def compute(bi, ready):
+            b = bufs[bi]
+            for ev in ready:
+                stream.wait_event(ev)
+            with torch.cuda.stream(stream):
+                if args.entry == "gemm":
+                    y = tq_gemm(b["x"], b["c"], b["s"], wl.k, L=wl.L)
+                elif args.entry == "packed":
+                    tq_packed([b["x"][a:e] for a, e in zip(offs[:-1], offs[1:])], b["c"], b["s"], wl.k, L=wl.L,
+                              outs=[ypk[a:e] for a, e in zip(offs[:-1], offs[1:])])
+                    y = ypk
+                elif args.entry == "gateup":
+                    y = tq_gateup(b["x"], b["c"], b["s"], b["cu"], b["su"], wl.k, L=wl.L)[2]   # the activation
+                else:
+                    y = tq_decode(b["c"], b["s"], wl.K, wl.k, L=wl.L)
+                hout.copy_(y, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                free[bi] = ev
+
+        def run_steps(n, start=None):
+            ready = upload(0, after=start)
+            for i in range(n):
+                nxt = upload((i + 1) % 2) if i + 1 < n else None
+                compute(i % 2, ready)
+                ready = nxt
+
+        run_steps(3)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(n_e2e):
-                e2e_step()
-            e1.record(stream)
+        e0.record(stream)
+        run_steps(n_e2e, start=e0)
+        e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / n_e2e
         (e2e_ms,) = max_over_ranks([e2e_ms], device="cuda")
         h2d = (hx.numel() * 2 if args.entry != "decode" else 0) + n_mats * (hc.numel() * 4 + hs.numel() * 2)
         e2e = {"value": round(whole_job_gbs(world, n_mats * wl.code_bytes, e2e_ms), 2), "unit": "GB/s",
                "us_per_call": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": hout.numel() * 2}
+               "d2h_bytes_per_step": hout.numel() * 2,
+               "pipelining": "two buffer sets: step i+1's uploads overlap step i's product"}
 
     # ---- roofline of the step's only kernel ----
     peaks, peak_src = measured_peaks()
