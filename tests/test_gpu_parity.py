@@ -419,3 +419,91 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable(tq, oracle_lib):
     w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
     ref, refabs = oracle_gemm_par(oracle_lib, x, w)
     assert_gemm_close(got, ref, refabs, "after the self-test")
+
+
+def test_concurrent_streams_give_the_sequential_bits(tq):
+    """Calls on different streams, each with its own workspace, may overlap on
+    the GPU: small-M products on two streams and a tensor-core product on a
+    third, issued interleaved, give exactly the bits of the same calls run one
+    at a time (each product's summation order is fixed by its launch shape)."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    lib = binding.load()
+    cases = [(8, 1024, 3000, 3), (5, 2048, 1500, 2), (64, 1024, 2000, 4)]
+    data = []
+    for i, (M, K, N, k) in enumerate(cases):
+        x, codes, scales = _inputs(M, K, N, k, seed=9960 + i)
+        ws = torch.zeros(max(binding.gemm_workspace_bytes(M, K, N, k), 256), dtype=torch.uint8, device="cuda")
+        data.append((M, K, N, k, dev_bf16(x), dev_codes(codes), dev_bf16(scales), ws))
+
+    def call(d, out, stream):
+        M, K, N, k, dx, dc, ds, ws = d
+        rc = lib.trellis_gemm_ws(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256, out.data_ptr(),
+                                 ws.data_ptr(), ws.numel(), stream.cuda_stream)
+        assert rc == 0, binding.status_string(rc)
+
+    main = torch.cuda.current_stream()
+    want = []
+    for d in data:
+        o = torch.empty((d[0], d[2]), dtype=torch.bfloat16, device="cuda")
+        call(d, o, main)
+        torch.cuda.synchronize()
+        want.append(o.view(torch.int16).cpu().numpy())
+    streams = [torch.cuda.Stream() for _ in data]
+    outs = [[torch.empty((d[0], d[2]), dtype=torch.bfloat16, device="cuda") for _ in range(6)] for d in data]
+    torch.cuda.synchronize()
+    for rep in range(6):
+        for d, s, o in zip(data, streams, outs):
+            call(d, o[rep], s)
+    torch.cuda.synchronize()
+    assert lib.trellis_device_status(None) == 0
+    for i, o in enumerate(outs):
+        for rep in range(6):
+            assert np.array_equal(o[rep].view(torch.int16).cpu().numpy(), want[i]), (i, rep)
+
+
+def test_host_threads_on_their_own_streams(tq):
+    """Several host threads, each with its own stream and workspace, call the
+    library at once: every result equals the single-threaded one."""
+    import threading
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    lib = binding.load()
+    M, K, N, k = 8, 1024, 2500, 3
+    x, codes, scales = _inputs(M, K, N, k, seed=9970)
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    need = max(binding.gemm_workspace_bytes(M, K, N, k), 256)
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ws0 = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    assert lib.trellis_gemm_ws(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256, ref.data_ptr(),
+                               ws0.data_ptr(), need, torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    want = ref.view(torch.int16).cpu().numpy()
+    nthreads, reps = 4, 5
+    wss = [torch.zeros(need, dtype=torch.uint8, device="cuda") for _ in range(nthreads)]
+    outs = [[torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(reps)] for _ in range(nthreads)]
+    streams = [torch.cuda.Stream() for _ in range(nthreads)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(t):
+        try:
+            torch.cuda.set_device(0)
+            for r in range(reps):
+                rc = lib.trellis_gemm_ws(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256,
+                                         outs[t][r].data_ptr(), wss[t].data_ptr(), need, streams[t].cuda_stream)
+                if rc != 0:
+                    errors.append(rc)
+        except Exception as e:   # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(nthreads)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for t in range(nthreads):
+        for r in range(reps):
+            assert np.array_equal(outs[t][r].view(torch.int16).cpu().numpy(), want), (t, r)
