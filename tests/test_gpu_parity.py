@@ -507,3 +507,36 @@ def test_host_threads_on_their_own_streams(tq):
     for t in range(nthreads):
         for r in range(reps):
             assert np.array_equal(outs[t][r].view(torch.int16).cpu().numpy(), want), (t, r)
+
+
+@pytest.mark.parametrize("M,K,N,k", [(8, 1024, 3000, 3), (64, 1024, 2000, 4), (300, 512, 700, 2)])
+def test_cuda_graph_capture_replays_the_eager_bits(tq, M, K, N, k):
+    """trellis_gemm_ws captured into a CUDA graph (no allocation or host sync
+    inside the call; programmatic launches become graph edges) replays to the
+    bits of the eager call, on the CUDA-core and the tensor-core paths."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    lib = binding.load()
+    x, codes, scales = _inputs(M, K, N, k, seed=9980 + M)
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    ws = torch.zeros(max(binding.gemm_workspace_bytes(M, K, N, k), 256), dtype=torch.uint8, device="cuda")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+
+    def call(stream_handle):
+        return lib.trellis_gemm_ws(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, 12, 256,
+                                   out.data_ptr(), ws.data_ptr(), ws.numel(), stream_handle)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert call(s.cuda_stream) == 0
+    torch.cuda.synchronize()
+    want = out.view(torch.int16).cpu().numpy().copy()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        assert call(torch.cuda.current_stream().cuda_stream) == 0
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out.view(torch.int16).cpu().numpy(), want)
+    assert lib.trellis_device_status(None) == 0
