@@ -335,12 +335,24 @@ def run_ours(args, wl):
     time.sleep(0.15)
     if world > 1:
         dist.barrier()
+    graph = None
+    if args.graph:
+        # the K steps captured once into a CUDA graph (outside the timed region)
+        # and replayed inside it: the same launches, no host launch overhead
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                call(args.warmup + i)
+        torch.cuda.synchronize()
     torch.cuda.synchronize()
     t_host0 = time.perf_counter()
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for i in range(args.steps):
-            call(args.warmup + i)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                call(args.warmup + i)
         t_end.record(stream)
     torch.cuda.synchronize()
     t_host = time.perf_counter() - t_host0
@@ -551,6 +563,7 @@ def run_ours(args, wl):
         "config": {"workload": wl.name, "entry": "trellis_" + args.entry, "M": wl.M, "K": wl.K, "N": wl.N,
                    **({"groups": group_rows(wl.M, args.groups)} if args.entry == "packed" else {}),
                    "k": wl.k, "L": wl.L, "T": wl.T, "parallelism": f"replicas{world}",
+                   "launch": "CUDA graph of the K steps" if args.graph else "stream, programmatic launches",
                    "l2": f"rotating {n_rot} code copies ({n_rot * wl.code_bytes / 1e6:.0f} MB > 2x L2)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks, "host_wall_s": round(t_host, 3),
@@ -623,6 +636,8 @@ def main(argv=None):
                     help="time the fused product (default), the dense decode, the gate/up pair with its "
                          "activation, or the token-packed product of --groups sequences")
     ap.add_argument("--groups", type=int, default=4, help="sequences the M rows are split into (--entry packed)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the K timed steps into one CUDA graph and time its replay")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
