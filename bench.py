@@ -234,6 +234,13 @@ def oracle_throughput(wl, x, codes, scales, budget_s: float, threads: int, max_r
 
 
 # ---------------------------------------------------------------- our arm --
+def path_dtype(entry: str, M: int) -> str:
+    """The arithmetic the timed path computes in: the decode and the CUDA-core
+    product (M <= 16) multiply bf16-valued operands in fp32; on the tensor
+    cores (M > 16) the product is a bf16 MMA with fp32 accumulation."""
+    return "bf16" if entry != "decode" and M > 16 else "f32"
+
+
 def group_rows(M: int, groups: int) -> list[int]:
     """M rows split into `groups` sequences whose sizes differ by at most one."""
     if not 1 <= groups <= M:
@@ -559,7 +566,7 @@ def run_ours(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "us_per_call": round(ms_step * 1e3, 2), "isolated_call_us": round(isolated_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": path_dtype(args.entry, wl.M), "data": "synthetic",
         "config": {"workload": wl.name, "entry": "trellis_" + args.entry, "M": wl.M, "K": wl.K, "N": wl.N,
                    **({"groups": group_rows(wl.M, args.groups)} if args.entry == "packed" else {}),
                    "k": wl.k, "L": wl.L, "T": wl.T, "parallelism": f"replicas{world}",
@@ -614,7 +621,7 @@ def run_reference(args, wl):
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "k": wl.k, "L": wl.L, "T": wl.T,
                    "parallelism": "host cores"},
