@@ -119,3 +119,26 @@ def test_packed_python_api(tq, oracle_lib):
         ref, refabs = oracle_gemm_par(oracle_lib, x[pos:pos + r], w)
         assert_gemm_close(bits, ref, refabs)
         pos += r
+
+
+def test_packed_many_groups(tq, oracle_lib):
+    """100 groups (two gather and two scatter launches of at most 64 groups),
+    mostly single rows: every group matches the concatenated product bit for bit."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
+    lib = binding.load()
+    rng = np.random.default_rng(11)
+    rows = [int(r) for r in rng.integers(1, 4, 100)]
+    rows[:60] = [1] * 60
+    N, K, k = 220, 512, 3
+    M = sum(rows)
+    x, codes, scales = _inputs(M, K, N, k, seed=8500)
+    dx = dev_bf16(x)
+    offs = np.cumsum([0] + rows)
+    xs = [dx[a:b].contiguous() for a, b in zip(offs[:-1], offs[1:])]
+    dc, ds = dev_codes(codes), dev_bf16(scales)
+    ws = torch.zeros(binding.gemm_packed_workspace_bytes(rows, K, N, k), dtype=torch.uint8, device="cuda")
+    got = _run_packed(lib, xs, rows, dc, ds, K, N, k, 12, ws)
+    whole = tq.gemm(dx, dc, ds, k).view(torch.int16).cpu().numpy().view(np.uint16)
+    for g, (a, b) in enumerate(zip(offs[:-1], offs[1:])):
+        assert np.array_equal(got[g], whole[a:b]), g

@@ -95,3 +95,31 @@ def test_noalloc_rejects_geometry_beyond_its_scratch(lib):
     if found is None:
         pytest.skip("no accepted geometry needs more than 16 MiB of scratch on this device")
     assert lib.trellis_gemm_noalloc(FAKE, FAKE, FAKE, 16, 256, found, 4, 12, 256, FAKE, None) == -7
+
+
+@pytest.mark.parametrize("M,K,N,k,L", [(6, 1024, 3000, 5, 16), (40, 512, 1000, 1, 9)])
+def test_noalloc_general_geometry(lib, M, K, N, k, L):
+    """The no-allocation entry on a geometry outside k in {2,3,4}, L = 12, on
+    both paths, against trellis_gemm_ws within the product tolerance."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding, synth
+    x, codes, scales = synth.small(M, K, N, k, seed=4300 + M + k).generate()
+    dx, dc, ds = _dev(x, torch, True), _dev(codes, torch, False), _dev(scales, torch, True)
+    s = torch.cuda.current_stream().cuda_stream
+    need = binding.gemm_workspace_bytes(M, K, N, k, L)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert lib.trellis_gemm_ws(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, L, 256,
+                               ref.data_ptr(), ws.data_ptr(), ws.numel(), s) == 0
+    w = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    assert lib.trellis_decode(dc.data_ptr(), ds.data_ptr(), K, N, k, L, 256, w.data_ptr(), s) == 0
+    refabs = dx.double().abs() @ w.double().abs().T
+    reff = ref.double()
+    ulp = torch.exp2(torch.floor(torch.log2(reff.abs().clamp_min(2.0 ** -126))) - 7)
+    tol = torch.maximum(2 * ulp, 1e-4 * refabs)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc = lib.trellis_gemm_noalloc(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), M, K, N, k, L, 256,
+                                  out.data_ptr(), s)
+    assert rc == 0, binding.status_string(rc)
+    torch.cuda.synchronize()
+    assert bool(torch.all((out.double() - reff).abs() <= tol))
