@@ -297,13 +297,14 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                                  :: "r"(dst + (((a_chunk0 + q) ^ a_rsw) << 4)), "r"(packed[4 * q]),
                                     "r"(packed[4 * q + 1]), "r"(packed[4 * q + 2]), "r"(packed[4 * q + 3])
                                  : "memory");
-                if (kTcStages < 4 || (d & 1)) {
-                    // with four stages, stages come in pairs (K / 128 is even):
-                    // one proxy fence and both arrivals after the second
+                if (kTcStages < 3 || (d & 1)) {
+                    // with three or four stages, stages come in pairs (K / 128
+                    // is even): one proxy fence and both arrivals after the
+                    // second (two stages leave too little slack for it)
                     fence_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        if (kTcStages >= 4) mbar_arrive(bar_full + 8 * ((i - 1) % kTcStages));
+                        if (kTcStages >= 3) mbar_arrive(bar_full + 8 * ((i - 1) % kTcStages));
                         mbar_arrive(bar_full + 8 * s);
                     }
                 }
