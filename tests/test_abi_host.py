@@ -164,3 +164,30 @@ def test_packed_workspace_size_on_the_tensor_core_path(lib):
     assert lib.trellis_gemm_packed_workspace_size(one, 1, K, N, 4, 12, 256, ctypes.byref(n)) == 0
     assert n.value == 0    # one group runs in place on the tensor cores
     assert lib.trellis_gemm_packed_workspace_size(r, 2, K, N, 4, 12, 256, None) == -1
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++11")])
+def test_header_compiles_without_cuda_headers(tmp_path, lang, std):
+    """include/trellis.h is a plain C ABI: it compiles as C99 and as C++ with
+    no CUDA header on the include path, and its prototypes match pointers of
+    the documented types."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / "abi_check.c"
+    src.write_text(
+        '#include "trellis.h"\n'
+        "int main(void) {\n"
+        "    int (*gemm)(const uint16_t *, const uint32_t *, const uint16_t *, int, int, int, int, int, int,\n"
+        "                uint16_t *, cudaStream_t) = trellis_gemm;\n"
+        "    int (*dec)(const uint32_t *, const uint16_t *, int, int, int, int, int, uint16_t *,\n"
+        "               cudaStream_t) = trellis_decode;\n"
+        "    const char *(*name)(int) = trellis_status_string;\n"
+        "    (void)gemm; (void)dec; (void)name;\n"
+        "    return TRELLIS_OK;\n"
+        "}\n")
+    r = subprocess.run([cc, "-x", lang, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
