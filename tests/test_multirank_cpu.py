@@ -55,3 +55,28 @@ def test_whole_job_throughput_is_weak_scaling():
     one = bench.whole_job_gbs(1, 33_423_360, 0.1)
     assert one == pytest.approx(334.2336)
     assert bench.whole_job_gbs(4, 33_423_360, 0.1) == pytest.approx(4 * one)
+
+
+def test_reference_arm_prints_once_from_rank_zero():
+    """bench.py --impl reference launched as two ranks: rank 0 times the oracle
+    and prints one JSON line (impl reference, the oracle's own cpu_baseline and
+    e2e keys); rank 1 exits 0 without output."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    outs = []
+    for rank in (0, 1):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2",
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
+        r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                            "--warmup", "3", "--ref-budget", "0.5"], capture_output=True, text=True, env=env,
+                           cwd=root, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs.append([line for line in r.stdout.splitlines() if line.strip()])
+    assert outs[1] == []
+    assert len(outs[0]) == 1
+    line = json.loads(outs[0][0])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
