@@ -145,7 +145,10 @@ def pin_golden_worked_examples(o):
 def pin_window_bruteforce(o, seed=1234):
     """Windows against the explicit bit-string, on random and crafted single blocks."""
     rng = np.random.default_rng(seed)
-    for k, L in [(2, 12), (3, 12), (4, 12), (1, 12), (5, 12), (6, 16), (8, 16), (4, 24), (2, 9)]:
+    # the pages' k in {2,3,4} with L = 12, then the general geometry 1 <= k <= 8,
+    # k < L <= 24, including every k and the narrowest and widest windows
+    for k, L in [(2, 12), (3, 12), (4, 12), (1, 12), (5, 12), (6, 16), (8, 16), (4, 24), (2, 9),
+                 (7, 12), (7, 20), (1, 2), (1, 24), (8, 9), (8, 24), (3, 4)]:
         T = 256
         wpb = T * k // 32
         blocks = [rng.integers(0, 2 ** 32, wpb, dtype=np.uint64).astype(np.uint32) for _ in range(3)]
