@@ -202,13 +202,14 @@ def pin_bf16_rounding(o, seed=7):
 def pin_decode_composition(o, seed=99):
     """Whole decode of small matrices against the independent composition."""
     rng = np.random.default_rng(seed)
-    for k in (2, 3, 4):
+    # the pages' geometries, then the general-geometry reading (1 <= k <= 8, k < L <= 24)
+    for k, L in [(2, 12), (3, 12), (4, 12), (1, 12), (5, 16), (7, 20), (8, 24)]:
         N, K = 3, 512
         codes = rng.integers(0, 2 ** 32, (N, K * k // 32), dtype=np.uint64).astype(np.uint32)
         scales = bf16_bits_torch(rng.uniform(0.005, 0.02, N).astype(np.float32))
-        got = o.decode(codes, scales, K, N, k)
-        want = decode_independent(codes, scales, K, N, k)
-        assert np.array_equal(got, want), k
+        got = o.decode(codes, scales, K, N, k, L=L)
+        want = decode_independent(codes, scales, K, N, k, L=L)
+        assert np.array_equal(got, want), (k, L)
 
 
 def pin_scale_linearity(o, seed=5):
