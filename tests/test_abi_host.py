@@ -191,3 +191,21 @@ def test_header_compiles_without_cuda_headers(tmp_path, lang, std):
     r = subprocess.run([cc, "-x", lang, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
                         "-I", os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_abi_and_oracle_accept_the_same_geometries(lib):
+    """The library and the oracle agree on which (k, L, T) are valid: the ABI's
+    workspace query at M = 64 validates without touching a device, the oracle's
+    geometry check is its own code."""
+    import oracle
+    o = oracle.get()
+    n = ctypes.c_size_t(0)
+    for k in range(0, 10):
+        for L in range(0, 27):
+            for T in (128, 256, 512):
+                abi_ok = lib.trellis_gemm_workspace_size(64, 1024, 64, k, L, T, ctypes.byref(n)) == 0
+                oracle_ok = o.lib.oracle_check_geometry(1024, 64, k, L, T) == 0
+                if T == 256:
+                    assert abi_ok == oracle_ok, (k, L, T)
+                else:
+                    assert not abi_ok, (k, L, T)   # the library takes the pages' block length only
