@@ -11,6 +11,8 @@ import os
 
 import numpy as np
 
+import oracle
+
 
 def dev_bf16(bits: np.ndarray):
     import torch
@@ -31,10 +33,9 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32)
 
 
-def ulp_bf16_of(v: np.ndarray) -> np.ndarray:
-    """Spacing of bf16 values at |v| (the smallest normal spacing below 2^-126)."""
-    a = np.maximum(np.abs(np.asarray(v, dtype=np.float64)), 2.0 ** -126)
-    return np.exp2(np.floor(np.log2(a)) - 7)
+# the spacing of bf16 values at |v| (the smallest normal spacing below 2^-126):
+# the oracle's, pinned in test_tolerance_pins.py
+ulp_bf16_of = oracle.ulp_bf16
 
 
 def _threads() -> int:
@@ -65,7 +66,6 @@ def oracle_gemm_par(o, x, w_rows):
 
 def assert_gemm_close(got_bits: np.ndarray, ref: np.ndarray, refabs: np.ndarray, what: str = ""):
     """|gpu - ref| <= max(2 bf16 ulp of ref, 1e-4 * sum_k |w x|), element by element."""
-    import oracle
     got = bf16_to_f32(got_bits).astype(np.float64)
     tol = oracle.gemm_tolerance(ref, refabs)
     err = np.abs(got - ref.astype(np.float64))
