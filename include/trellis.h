@@ -115,14 +115,25 @@ int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, 
  * workspace and its waits are bounded (see trellis_device_status).
  *
  * The summation order is fixed by the launch geometry, so repeated calls on
- * the same device give identical bits.  The kernel balances work across all
- * SMs by splitting rows' K-ranges across CTAs; the split partial sums go
- * through a workspace.  trellis_gemm uses a workspace owned by the library:
- * the first call on each device allocates it (cudaMalloc, then zero-filled),
- * later calls reuse it, so that first call must not happen during stream
- * capture, and calls that use it must not overlap on the GPU (use
- * trellis_gemm_ws with separate workspaces for concurrent streams).
- * Errors: as trellis_decode, plus M outside 1..65536 -> TRELLIS_ERR_UNSUPPORTED.
+ * the same device give identical bits (the bits of trellis_gemm_ws).  For
+ * M <= 16 the kernel balances work across all SMs by splitting rows' K-ranges
+ * across CTAs; the split partial sums go through scratch memory.  trellis_gemm
+ * takes that scratch from a fixed 4 MiB region of static device memory in the
+ * library image (zero when loaded; every completed call leaves it ready for
+ * the next).  The call itself never allocates and never synchronises: the
+ * only host-side step is a one-time lookup of the region's address on each
+ * device.  Under the CUDA runtime's default lazy module loading the driver
+ * places the region and the kernels' code in device memory when a call first
+ * needs them, and that load can wait for work in flight on the device; make
+ * the first call per device (and bit width) before any stream capture and
+ * before latency-sensitive work, or run with CUDA_MODULE_LOADING=EAGER, under
+ * which the library's modules are loaded with it and even the first call
+ * neither allocates nor waits.  All trellis_gemm calls on a device share the
+ * region: calls that may overlap on the GPU (on two streams) race; use
+ * trellis_gemm_ws with a workspace per stream for concurrent calls.
+ * Errors: as trellis_decode, plus M outside 1..65536 -> TRELLIS_ERR_UNSUPPORTED;
+ * on a device with more than 256 SMs the region is too small for M <= 16 ->
+ * TRELLIS_ERR_WORKSPACE (use trellis_gemm_ws).
  */
 int trellis_gemm(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M, int K,
                  int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
@@ -226,10 +237,18 @@ int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T,
  * The first call on each device does a one-time set-up with that device
  * current (it looks up the array's device address and clears its counter
  * region, synchronising the device); make that first call before any stream
- * capture.  Every call shares the array: calls that may overlap on the same
- * GPU (for instance on two streams) race and must be serialised by the caller.
- * Geometries whose scratch (as reported by trellis_gemm_workspace_size) exceeds
- * 16 MiB are rejected with TRELLIS_ERR_WORKSPACE before any launch.
+ * capture.  Under the CUDA runtime's default lazy module loading, the array
+ * and the kernels' code are placed in device memory when that first call
+ * touches them, not when the library is loaded: a process that reserves all
+ * free device memory up front must make its first call (per device and per
+ * bit width k, whose kernels are separate modules) before reserving, or run
+ * with CUDA_MODULE_LOADING=EAGER.  Every call shares the array: calls that may
+ * overlap on the same GPU (for instance on two streams) race and must be
+ * serialised by the caller.  Same argument checks, in the same order, as
+ * trellis_gemm; then geometries whose scratch (as reported by
+ * trellis_gemm_workspace_size) exceeds 16 MiB are rejected with
+ * TRELLIS_ERR_WORKSPACE before any launch (a guard for devices with more than
+ * 1280 SMs: below that the scratch of every accepted geometry fits).
  */
 int trellis_gemm_noalloc(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
                          int K, int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);

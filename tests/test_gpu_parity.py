@@ -236,7 +236,7 @@ def test_gemm_deterministic(tq):
 
 
 def test_gemm_library_workspace_matches(tq):
-    """trellis_gemm (library-owned workspace) equals trellis_gemm_ws (caller's)."""
+    """trellis_gemm (the library's static scratch) equals trellis_gemm_ws (caller's)."""
     import torch
     from trellis_quantized_weight_gb300 import binding
     M, K, N, k = 5, 2048, 2000, 2
@@ -354,11 +354,24 @@ def test_full_decode_bitexact(tq, oracle_lib, full_inputs, name):
 
 @pytest.mark.parametrize("name", ALL_WORKLOADS)
 def test_full_gemm(tq, oracle_lib, full_inputs, name):
+    """Both product entries at full size against the oracle: trellis_gemm_ws (the
+    caller's workspace, through the Python API) and trellis_gemm (no workspace
+    argument, the library's static scratch), which must also agree bit for bit."""
+    import torch
+    from trellis_quantized_weight_gb300 import binding
     wl, x, codes, scales = full_inputs(name)
-    got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), wl.k))
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    got = host_bits(tq.gemm(dx, dc, ds, wl.k))
+    out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+    rc = binding.abi_gemm(dx.data_ptr(), dc.data_ptr(), ds.data_ptr(), wl.M, wl.K, wl.N, wl.k, 12, 256,
+                          out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, binding.status_string(rc)
+    got_abi = host_bits(out)
     w = oracle_decode_par(oracle_lib, codes, scales, wl.K, wl.N, wl.k)
     ref, refabs = oracle_gemm_par(oracle_lib, x, w)
     assert_gemm_close(got, ref, refabs, name)
+    assert_gemm_close(got_abi, ref, refabs, name + " (trellis_gemm)")
+    assert np.array_equal(got, got_abi)
 
 
 def test_gemm_largest_m(tq, oracle_lib):

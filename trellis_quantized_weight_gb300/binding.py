@@ -142,18 +142,25 @@ def _require(t, name, dtypes, ndim):
 
 
 _ws_cache: dict = {}
+_ws_lock = threading.Lock()
 
 
-def _workspace(device, nbytes: int):
-    """A zero-filled torch buffer reused across calls on one device (grown as needed)."""
+def _workspace(device, nbytes: int, stream=None):
+    """A zero-filled torch buffer per (device, stream), reused across calls and grown
+    as needed.  It is allocated and zero-filled on the stream the calls run on, so
+    stream order alone makes the fill land first and lets torch's caching allocator
+    recycle an outgrown buffer once the calls enqueued before it are done: no host
+    synchronisation.  One buffer per stream also keeps calls on different streams
+    off each other's split-K counters."""
     torch = _torch()
-    key = torch.device(device).index
-    buf = _ws_cache.get(key)
-    if buf is None or buf.numel() < nbytes:
-        torch.cuda.synchronize(device)
-        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
-        torch.cuda.synchronize(device)   # the fill must land before any stream uses it
-        _ws_cache[key] = buf
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    key = (torch.device(device).index, s.cuda_stream)
+    with _ws_lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < nbytes:
+            with torch.cuda.stream(s):
+                buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+            _ws_cache[key] = buf
     return buf
 
 
@@ -192,7 +199,7 @@ def gemm(x, codes, scales, k: int, L: int = 12, T: int = 256, out=None, stream=N
     if tuple(out.shape) != (M, N):
         raise ValueError("out must be [M, N]")
     nbytes = gemm_workspace_bytes(M, K, N, k, L, T)
-    ws = _workspace(x.device, max(nbytes, 256))
+    ws = _workspace(x.device, max(nbytes, 256), stream)
     rc = abi_gemm_ws(x.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, K, N, k, L, T,
                      out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(x.device, stream))
     _check(rc, "trellis_gemm_ws")
@@ -218,7 +225,7 @@ def gemm_gateup(x, codes_gate, scales_gate, codes_up, scales_up, k: int, act: bo
     u = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     a = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if act else None
     nbytes = gemm_gateup_workspace_bytes(M, K, N, k, L, T)
-    ws = _workspace(x.device, max(nbytes, 256))
+    ws = _workspace(x.device, max(nbytes, 256), stream)
     rc = load().trellis_gemm_gateup(x.data_ptr(), codes_gate.data_ptr(), scales_gate.data_ptr(),
                                     codes_up.data_ptr(), scales_up.data_ptr(), M, K, N, k, L, T,
                                     g.data_ptr(), u.data_ptr(), a.data_ptr() if act else None,
@@ -251,7 +258,7 @@ def gemm_packed(xs, codes, scales, k: int, L: int = 12, T: int = 256, outs=None,
         if tuple(o.shape) != (r, N):
             raise ValueError(f"outs[{i}] must be [{r}, {N}]")
     nbytes = gemm_packed_workspace_bytes(rows, K, N, k, L, T)
-    ws = _workspace(xs[0].device, max(nbytes, 256))
+    ws = _workspace(xs[0].device, max(nbytes, 256), stream)
     xp = (ctypes.c_void_p * len(xs))(*[x.data_ptr() for x in xs])
     op = (ctypes.c_void_p * len(outs))(*[o.data_ptr() for o in outs])
     rp = (ctypes.c_int * len(rows))(*rows)

@@ -65,20 +65,20 @@ int noalloc_device(NoAllocDevice& out) {
     return TRELLIS_OK;
 }
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
-
 }  // namespace
 
 extern "C" int trellis_gemm_noalloc(const uint16_t* x, const uint32_t* codes, const uint16_t* scales,
                                     int M, int K, int N, int k, int L, int T, uint16_t* out,
                                     cudaStream_t stream) {
-    if (x == nullptr || codes == nullptr || scales == nullptr || out == nullptr) return TRELLIS_ERR_NULL;
-    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 2) || !aligned(out, 2))
-        return TRELLIS_ERR_ALIGN;
-    size_t need = 0;
-    int rc = trellis_gemm_workspace_size(M, K, N, k, L, T, &need);   // validates the geometry
+    int rc = trellis::check_gemm(x, codes, scales, M, K, N, k, L, T, out);   // as trellis_gemm
     if (rc != TRELLIS_OK) return rc;
-    if (need > kNoAllocScratchBytes) return TRELLIS_ERR_WORKSPACE;   // beyond the fixed array
+    size_t need = 0;
+    rc = trellis_gemm_workspace_size(M, K, N, k, L, T, &need);
+    if (rc != TRELLIS_OK) return rc;
+    // Beyond the fixed array.  Defensive: the scratch grows with the SM count
+    // (1 MiB of counters plus at most 12 KiB a CTA), so no accepted geometry
+    // exceeds 16 MiB on a device with at most 1280 SMs.
+    if (need > kNoAllocScratchBytes) return TRELLIS_ERR_WORKSPACE;
     if (M > 16) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, L, out, stream);   // no scratch
     NoAllocDevice d;
     rc = noalloc_device(d);

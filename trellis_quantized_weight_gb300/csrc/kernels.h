@@ -62,6 +62,21 @@ cudaError_t launch_programmatic(void (*kernel)(Params...), unsigned grid, unsign
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// The argument checks of trellis_gemm, in its order (pointers, codes and
+// scales, geometry, M, then the alignment of x and out); returns 0 or a
+// trellis_status.  Shared by every entry point that takes trellis_gemm's
+// arguments, so each rejects a call the same way.
+int check_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N, int k,
+               int L, int T, const uint16_t* out);
+
+// trellis_gemm's split-K scratch: a static device array of kGemmScratchBytes
+// (1 MiB of tile counters, then partial sums), zero when loaded and left with
+// zero counters by every completed call.  Writes its address on the current
+// device to *ptr; no allocation, no synchronisation.  Returns 0 or a
+// trellis_status.
+constexpr size_t kGemmScratchBytes = size_t(4) << 20;
+int gemm_static_scratch(void** ptr);
+
 // Dense decode of all N rows into out [N, K].  Returns 0 or a trellis_status.
 int launch_decode(const uint32_t* codes, const uint16_t* scales, int K, int N, int k, int L,
                   uint16_t* out, cudaStream_t stream, const DeviceInfo& dev);

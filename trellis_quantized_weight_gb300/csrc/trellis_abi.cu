@@ -63,6 +63,11 @@ int check_codes(const uint32_t* codes, const uint16_t* scales) {
     return TRELLIS_OK;
 }
 
+
+}  // namespace
+
+namespace trellis {
+
 int check_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
                int k, int L, int T, const uint16_t* out) {
     if (x == nullptr || out == nullptr) return TRELLIS_ERR_NULL;
@@ -75,37 +80,11 @@ int check_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scales,
     return TRELLIS_OK;
 }
 
-// Library-owned workspace of trellis_gemm, one per device, grown on demand.
-struct OwnedWorkspace {
-    void* ptr = nullptr;
-    size_t bytes = 0;
-};
+}  // namespace trellis
 
-int owned_workspace(const DeviceInfo& dev, size_t need, void** ptr) {
-    static std::mutex mu;
-    static OwnedWorkspace ws[kMaxDevices];
-    std::lock_guard<std::mutex> lock(mu);
-    OwnedWorkspace& w = ws[dev.device];
-    if (w.bytes < need) {
-        // growing: wait for work that may still use the old buffer
-        if (w.ptr != nullptr) {
-            if (cudaDeviceSynchronize() != cudaSuccess) return TRELLIS_ERR_CUDA;
-            cudaFree(w.ptr);
-            w.ptr = nullptr;
-            w.bytes = 0;
-        }
-        void* p = nullptr;
-        if (cudaMalloc(&p, need) != cudaSuccess) return TRELLIS_ERR_CUDA;
-        if (cudaMemset(p, 0, need) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
-            cudaFree(p);
-            return TRELLIS_ERR_CUDA;
-        }
-        w.ptr = p;
-        w.bytes = need;
-    }
-    *ptr = w.ptr;
-    return TRELLIS_OK;
-}
+namespace {
+
+using trellis::check_gemm;
 
 }  // namespace
 
@@ -184,10 +163,12 @@ int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scale
     if (rc != TRELLIS_OK) return rc;
     const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, L, dev);
     if (need == 0) return TRELLIS_ERR_SHAPE;
+    if (need > trellis::kGemmScratchBytes) return TRELLIS_ERR_WORKSPACE;   // more than 256 SMs
     void* ws = nullptr;
-    rc = owned_workspace(dev, need, &ws);
+    rc = trellis::gemm_static_scratch(&ws);
     if (rc != TRELLIS_OK) return rc;
-    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, L, out, ws, need, stream, dev);
+    return trellis::launch_gemm_smallm(x, codes, scales, M, K, N, k, L, out, ws, trellis::kGemmScratchBytes,
+                                       stream, dev);
 }
 
 int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T, size_t* bytes) {
