@@ -2,22 +2,26 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--entry gemm|decode|gateup|packed] [--rows M]
-                    [--bits k] [--window L]
+                    [--bits k] [--window L] [--no-per-config]
 
 One step = one fused decode-and-multiply call (trellis_gemm: code fetch,
-window, hash, quotient, scale/bf16 round, M-row FMA, reduction and bf16 store)
-on the headline workload: M=8 activation rows, K=5120, N=17408, k=3 bits, L=12,
-T=256, seeded synthetic inputs.  Metric: packed-weight GB/s (code bytes per
-second, whole job); the JSON line also carries us/call and the roofline
-fraction of the kernel.
+window, hash, quotient, scale/bf16 round, the product and the bf16 store) on
+the headline workload, the largest of the quantised-linear shapes: M=64
+activation rows, K=5120, N=17408, k=4 bits, L=12, T=256 (tensor cores),
+seeded synthetic inputs.  Metric: us/call and packed-weight GB/s (code bytes
+per second, whole job) with the kernel's roofline fraction.  The same JSON
+line carries `per_config`: every quantised-linear workload (M = 5, 8, 15, 1,
+64) and the dense decode, each timed in its own region of the same process,
+each with its roofline fraction, clocks and the oracle's CPU rate on all host
+cores and on one pinned core.
 
 Timing: W warm-up steps, then K steps bracketed by a barrier and
-torch.cuda.synchronize(), CUDA events on the launching stream around every
-call, max over ranks.  Between steps the code buffers rotate through enough
-independent copies that the set exceeds twice the L2, so every call streams
-its codes from HBM.  GPU clocks are sampled with nvidia-smi during the timed
-region.  Multi-GPU runs (torchrun) are independent replicas of the workload,
-one per rank (weak scaling, no data-path collective).
+torch.cuda.synchronize(), CUDA events on the launching stream around the K
+back-to-back calls, max over ranks.  Between steps the code buffers rotate
+through enough independent copies that the set exceeds twice the L2, so every
+call streams its codes from HBM.  GPU clocks are sampled with nvidia-smi during
+each timed region.  Multi-GPU runs (torchrun) are independent replicas of the
+workload, one per rank (weak scaling, no data-path collective).
 
 --impl reference times the CPU oracle (test infrastructure) on the host cores
 on a bounded sample of the same workload; it is a deliberately slow baseline.
@@ -46,8 +50,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-HEADLINE = "gemm_m8_k5120_n17408_k3"
-METRIC = "trellis GEMM packed-weight GB/s"
+# the largest of the quantised-linear workloads: 64 activation rows (tensor cores)
+HEADLINE = "prefill_m64_k5120_n17408_k4"
+METRIC = "trellis GEMM us/call & packed-weight GB/s (% of GB300 roofline)"
 METRIC_DECODE = "trellis decode packed-weight GB/s"
 METRIC_GATEUP = "trellis gate/up GEMM packed-weight GB/s"
 METRIC_PACKED = "trellis token-packed GEMM packed-weight GB/s"
@@ -201,38 +206,6 @@ def to_dev(bits: np.ndarray, torch, dtype):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).cuda()
 
 
-# ------------------------------------------------------------- CPU oracle --
-def oracle_throughput(wl, x, codes, scales, budget_s: float, threads: int, max_rows: int | None = None):
-    """Run the unchanged oracle (decode + product) over row chunks on `threads`
-    host threads for about budget_s seconds; returns (GB/s of codes, rows, s)."""
-    import oracle
-    o = oracle.get()
-    rows_total = wl.N if max_rows is None else min(wl.N, max_rows)
-    chunk = max(1, min(rows_total, 64))
-
-    def work(r):
-        w = o.decode(codes, scales, wl.K, wl.N, wl.k, L=wl.L, rows=r)
-        o.gemm_dense(x, w)
-        return r[1] - r[0]
-
-    done_rows = 0
-    t0 = time.perf_counter()
-    with cf.ThreadPoolExecutor(threads) as ex:
-        n0 = 0
-        while True:
-            batch = []
-            for _ in range(threads):
-                n1 = min(rows_total, n0 + chunk)
-                batch.append((n0, n1))
-                n0 = 0 if n1 >= rows_total else n1
-            done_rows += sum(ex.map(work, batch))
-            if time.perf_counter() - t0 >= budget_s:
-                break
-    dt = time.perf_counter() - t0
-    gbs = done_rows * wl.row_words * 4 / dt / 1e9
-    return gbs, done_rows, dt
-
-
 # ---------------------------------------------------------------- our arm --
 def path_dtype(entry: str, M: int) -> str:
     """The arithmetic the timed path computes in: the decode and the CUDA-core
@@ -248,6 +221,306 @@ def group_rows(M: int, groups: int) -> list[int]:
     return [M // groups + (1 if g < M % groups else 0) for g in range(groups)]
 
 
+def launches_per_step(entry: str, M: int, groups: int = 1) -> int:
+    """Our kernels one step launches: on the tensor cores one launch per matrix
+    for M <= 256, else one per 256-row chunk; otherwise one small-M launch; plus
+    the gate/up activation, or the packing's gather and scatter."""
+    n_mats = 2 if entry == "gateup" else 1
+    if entry != "decode" and M > 16:
+        n = n_mats * max(1, (M + 255) // 256)
+    else:
+        n = 1
+    if entry == "gateup":
+        n += 1
+    if entry == "packed" and groups > 1:   # the gather and the scatter, per 64 groups
+        n += 2 * ((groups + 63) // 64)
+    return n
+
+
+def roofline(wl, entry: str, kernel_ms: float, num_sms: int):
+    """The roofline of one step's kernel(s): time = max(bytes / HBM peak,
+    ops / ALU peak[, tensor FLOP / tensor peak]); achieved over peak for the
+    binding bound."""
+    peaks, peak_src = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz") or 2070.0)
+    hbm_peak = float(peaks["hbm_gbs"])
+    alu_peak = num_sms * ALU_LANES_PER_SM * sm_max * 1e6 / 1e12   # Tops/s
+    tensor_peak = float(peaks.get("bf16_tflops") or 1900.0)
+    n_mats = 2 if entry == "gateup" else 1
+    t_kernel = kernel_ms * 1e-3
+    flops = 0
+    if entry in ("gemm", "gateup", "packed") and wl.M > 16:
+        # tensor-core path: the decode runs on the ALUs, the M FMAs per weight
+        # are a dense bf16 contraction on the tensor cores
+        ops = n_mats * wl.weights * DECODE_OPS_PER_WEIGHT
+        flops = n_mats * 2 * wl.M * wl.N * wl.K
+        hbm_bytes = n_mats * (wl.code_bytes + wl.M * wl.N * 2) + wl.M * wl.K * 2
+        kernel_name = "gemm_tc"
+    elif entry in ("gemm", "gateup", "packed"):
+        # gate/up: both matrices in one launch, plus the elementwise activation
+        # (read 2 and write 1 bf16 [M, N]; bytes counted, no ALU ops)
+        ops = n_mats * wl.weights * (DECODE_OPS_PER_WEIGHT + wl.M)
+        hbm_bytes = n_mats * (wl.code_bytes + wl.M * wl.N * 2) + wl.M * wl.K * 2
+        if entry == "gateup":
+            hbm_bytes += 3 * wl.M * wl.N * 2
+        kernel_name = "gemm_smallm"
+    else:
+        ops = wl.weights * DECODE_OPS_PER_WEIGHT
+        hbm_bytes = wl.code_bytes + wl.weights * 2
+        kernel_name = "decode"
+    achieved_all = {"alu": ops / t_kernel / 1e12, "hbm": hbm_bytes / t_kernel / 1e9,
+                    "tensor": flops / t_kernel / 1e12}
+    t_roof = {"alu": ops / (alu_peak * 1e12), "hbm": hbm_bytes / (hbm_peak * 1e9),
+              "tensor": flops / (tensor_peak * 1e12)}
+    bound = max(t_roof, key=t_roof.get)
+    peak = {"alu": alu_peak, "hbm": hbm_peak, "tensor": tensor_peak}[bound]
+    achieved = achieved_all[bound]
+    return {"bound": bound,
+            "achieved": round(achieved, 3),
+            "peak": round(peak, 3),
+            "unit": {"alu": "Tops/s", "hbm": "GB/s", "tensor": "TFLOP/s"}[bound],
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(kernel_name, wl.name),
+            "peak_source": {"alu": f"{peak_src}: {num_sms} SMs x {ALU_LANES_PER_SM} lanes x "
+                                   f"{sm_max:.0f} MHz (of measured max clock)",
+                            "hbm": f"{peak_src} hbm_gbs (of measured)",
+                            "tensor": f"{peak_src} bf16_tflops (of measured)"}[bound],
+            "tensor_TFLOPs": round(achieved_all["tensor"], 1) if flops else None,
+            "ops_per_launch": ops, "algorithmic_bytes_per_launch": hbm_bytes,
+            "hbm_GBps": round(achieved_all["hbm"], 1),
+            "hbm_frac": round(achieved_all["hbm"] / hbm_peak, 4),
+            "alu_frac": round(achieved_all["alu"] / alu_peak, 4),
+            "roofline_us": round(max(t_roof.values()) * 1e6, 2),
+            "kernel_us": round(kernel_ms * 1e3, 2)}
+
+
+class Entry:
+    """One workload on one entry point, device-resident and ready to time: the
+    codes rotate through enough independent copies (> 2x L2) that every call
+    streams them from HBM."""
+
+    def __init__(self, wl, entry: str, lib, torch, stream, groups: int = 4):
+        from trellis_quantized_weight_gb300 import binding, synth
+        self.wl, self.entry = wl, entry
+        self.x, self.codes, self.scales = wl.generate()
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+        self.n_rot = n_rot = max(2, math.ceil(2 * l2 / wl.code_bytes) + 1)
+        self.n_mats = 2 if entry == "gateup" else 1
+        self.groups = groups
+        self.launches = launches_per_step(entry, wl.M, groups)
+        dx = self.dx = to_dev(self.x, torch, "bf16")
+        dscales = self.dscales = to_dev(self.scales, torch, "bf16")
+        dcodes = self.dcodes = [to_dev(self.codes, torch, "u32") for _ in range(n_rot)]
+        s_handle = stream.cuda_stream
+        self.codes_u = self.scales_u = None
+        if entry == "gateup":
+            # the up projection: a second matrix of the same shape, its own seed
+            _, self.codes_u, self.scales_u = synth.small(wl.M, wl.K, wl.N, wl.k, seed=wl.seed + 0x1000,
+                                                         sigma=wl.sigma).generate()
+            dcodes_u = [to_dev(self.codes_u, torch, "u32") for _ in range(n_rot)]
+            dscales_u = to_dev(self.scales_u, torch, "bf16")
+            outs = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+            ws_bytes = binding.gemm_gateup_workspace_bytes(wl.M, wl.K, wl.N, wl.k, wl.L)
+            ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+
+            def call(i):
+                rc = lib.trellis_gemm_gateup(dx.data_ptr(), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
+                                             dcodes_u[i % n_rot].data_ptr(), dscales_u.data_ptr(), wl.M, wl.K,
+                                             wl.N, wl.k, wl.L, wl.T, outs[0].data_ptr(), outs[1].data_ptr(),
+                                             outs[2].data_ptr(), ws.data_ptr(), ws.numel(), s_handle)
+                if rc != 0:
+                    raise RuntimeError(f"trellis_gemm_gateup failed: {binding.status_string(rc)}")
+        elif entry == "packed":
+            # the workload's M rows as `groups` sequences (sizes as equal as possible),
+            # gathered, multiplied once and scattered back by trellis_gemm_packed
+            rows = group_rows(wl.M, groups)
+            self.offs = offs = np.cumsum([0] + rows)
+            out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+            xp = (ctypes.c_void_p * len(rows))(*[dx[a:b].data_ptr() for a, b in zip(offs[:-1], offs[1:])])
+            op = (ctypes.c_void_p * len(rows))(*[out[a:b].data_ptr() for a, b in zip(offs[:-1], offs[1:])])
+            rp = (ctypes.c_int * len(rows))(*rows)
+            ws_bytes = binding.gemm_packed_workspace_bytes(rows, wl.K, wl.N, wl.k, wl.L)
+            ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+
+            def call(i):
+                rc = lib.trellis_gemm_packed(xp, rp, len(rows), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
+                                             wl.K, wl.N, wl.k, wl.L, wl.T, op, ws.data_ptr(), ws.numel(),
+                                             s_handle)
+                if rc != 0:
+                    raise RuntimeError(f"trellis_gemm_packed failed: {binding.status_string(rc)}")
+        elif entry == "gemm":
+            # trellis_gemm: the library's own split-K scratch, no workspace argument
+            out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+
+            def call(i):
+                rc = lib.trellis_gemm(dx.data_ptr(), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
+                                      wl.M, wl.K, wl.N, wl.k, wl.L, wl.T, out.data_ptr(), s_handle)
+                if rc != 0:
+                    raise RuntimeError(f"trellis_gemm failed: {binding.status_string(rc)}")
+        else:
+            wout = torch.empty((wl.N, wl.K), dtype=torch.bfloat16, device="cuda")
+
+            def call(i):
+                rc = lib.trellis_decode(dcodes[i % n_rot].data_ptr(), dscales.data_ptr(), wl.K, wl.N, wl.k,
+                                        wl.L, wl.T, wout.data_ptr(), s_handle)
+                if rc != 0:
+                    raise RuntimeError(f"trellis_decode failed: {binding.status_string(rc)}")
+        self.call = call
+
+    def config(self, world: int, graph: bool = False) -> dict:
+        wl = self.wl
+        return {"workload": wl.name, "entry": "trellis_" + self.entry, "M": wl.M, "K": wl.K, "N": wl.N,
+                **({"groups": group_rows(wl.M, self.groups)} if self.entry == "packed" else {}),
+                "k": wl.k, "L": wl.L, "T": wl.T, "parallelism": f"replicas{world}",
+                "launch": "CUDA graph of the K steps" if graph else "stream, programmatic launches",
+                "l2": f"rotating {self.n_rot} code copies ({self.n_rot * wl.code_bytes / 1e6:.0f} MB > 2x L2)"}
+
+
+def time_steps(ent, steps: int, warmup: int, stream, torch, world: int, gpu_index: int, graph: bool = False):
+    """W warm-up calls, then `steps` calls back to back on one stream (as a model
+    issues its layers) between one pair of CUDA events, with barriers and
+    synchronisation on both sides and nvidia-smi sampling the clocks.  Returns
+    (ms per step, clocks, host wall seconds)."""
+    import torch.distributed as dist
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            ent.call(i)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.15)
+    if world > 1:
+        dist.barrier()
+    g = None
+    if graph:
+        # the K steps captured once into a CUDA graph (outside the timed region)
+        # and replayed inside it: the same launches, no host launch overhead
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                ent.call(warmup + i)
+        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    t_host0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(steps):
+                ent.call(warmup + i)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    t_host = time.perf_counter() - t_host0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    return t_start.elapsed_time(t_end) / steps, clocks, t_host
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def host_cores() -> list[int]:
+    """The cores this process may run on."""
+    try:
+        return sorted(os.sched_getaffinity(0))
+    except AttributeError:
+        return list(range(os.cpu_count() or 1))
+
+
+def oracle_rate(wl, x, codes, scales, budget_s: float, threads: int, decode_only: bool = False,
+                pin_core: int | None = None):
+    """The unchanged oracle (decode + product, or decode alone) over row chunks on
+    `threads` host threads for about budget_s seconds.  With pin_core the work
+    runs in this thread alone, pinned to that core.  Returns (GB/s of codes,
+    microseconds per whole call extrapolated from the rows done, rows, seconds)."""
+    import oracle
+    o = oracle.get()
+    chunk = max(1, min(wl.N, 16 if pin_core is not None else 64))
+
+    def work(r):
+        w = o.decode(codes, scales, wl.K, wl.N, wl.k, L=wl.L, rows=r)
+        if not decode_only:
+            o.gemm_dense(x, w)
+        return r[1] - r[0]
+
+    done_rows = 0
+    n0 = 0
+    if pin_core is not None:
+        old = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, {pin_core})
+        try:
+            t0 = time.perf_counter()
+            while True:
+                n1 = min(wl.N, n0 + chunk)
+                done_rows += work((n0, n1))
+                n0 = 0 if n1 >= wl.N else n1
+                if time.perf_counter() - t0 >= budget_s:
+                    break
+            dt = time.perf_counter() - t0
+        finally:
+            os.sched_setaffinity(0, old)
+    else:
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(threads) as ex:
+            while True:
+                batch = []
+                for _ in range(threads):
+                    n1 = min(wl.N, n0 + chunk)
+                    batch.append((n0, n1))
+                    n0 = 0 if n1 >= wl.N else n1
+                done_rows += sum(ex.map(work, batch))
+                if time.perf_counter() - t0 >= budget_s:
+                    break
+        dt = time.perf_counter() - t0
+    gbs = done_rows * wl.row_words * 4 / dt / 1e9
+    us_call = dt / done_rows * wl.N * 1e6
+    return gbs, us_call, done_rows, dt
+
+
+def cpu_baseline_for(wl, x, codes, scales, budget_s: float, decode_only: bool = False) -> dict:
+    """The oracle on all host cores and on one pinned core, with the CPU model."""
+    cores = host_cores()
+    gbs, us, rows, dt = oracle_rate(wl, x, codes, scales, budget_s, len(cores), decode_only)
+    gbs1, us1, rows1, dt1 = oracle_rate(wl, x, codes, scales, budget_s, 1, decode_only, pin_core=cores[0])
+    what = "decode" if decode_only else "decode + product"
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": len(cores), "kind": "oracle",
+            "us_per_call": round(us, 1),
+            "sample": f"{rows} rows x K={wl.K} of {wl.name} ({what}) in {dt:.1f} s on {len(cores)} threads",
+            "one_core": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1, "us_per_call": round(us1, 1),
+                         "sample": f"{rows1} rows ({what}) in {dt1:.1f} s, pinned to core {cores[0]}"},
+            "cpu_model": cpu_model()}
+
+
+# The per-configuration table: every quantised-linear workload through
+# trellis_gemm, and the dense decode of the k = 3 and k = 4 weights.
+PER_CONFIG = [(name, "gemm") for name in
+              ["gemm_m5_k5120_n17408_k2", "gemm_m8_k5120_n17408_k3", "gemm_m15_k5120_n17408_k4",
+               "gemv_m1_k17408_n5120_k4", "prefill_m64_k5120_n17408_k4"]] + \
+             [("gemm_m8_k5120_n17408_k3", "decode"), ("prefill_m64_k5120_n17408_k4", "decode")]
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -257,117 +530,16 @@ def run_ours(args, wl):
     if world > 1 and not dist.is_initialized():
         dist.init_process_group("nccl")
 
-    from trellis_quantized_weight_gb300 import binding, build
+    from trellis_quantized_weight_gb300 import binding, build, synth
     build.build()
     lib = binding.load()
-
-    x, codes, scales = wl.generate()
     props = torch.cuda.get_device_properties(local)
-    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
-    n_rot = max(2, math.ceil(2 * l2 / wl.code_bytes) + 1)
-    dx = to_dev(x, torch, "bf16")
-    dscales = to_dev(scales, torch, "bf16")
-    dcodes = [to_dev(codes, torch, "u32") for _ in range(n_rot)]
     stream = torch.cuda.Stream()
-    s_handle = stream.cuda_stream
-    n_mats = 2 if args.entry == "gateup" else 1
-    if args.entry == "gateup":
-        # the up projection: a second matrix of the same shape, its own seed
-        from trellis_quantized_weight_gb300 import synth
-        _, codes_u, scales_u = synth.small(wl.M, wl.K, wl.N, wl.k, seed=wl.seed + 0x1000,
-                                           sigma=wl.sigma).generate()
-        dcodes_u = [to_dev(codes_u, torch, "u32") for _ in range(n_rot)]
-        dscales_u = to_dev(scales_u, torch, "bf16")
-        outs = [torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
-        ws_bytes = binding.gemm_gateup_workspace_bytes(wl.M, wl.K, wl.N, wl.k, wl.L)
-        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
 
-        def call(i):
-            rc = lib.trellis_gemm_gateup(dx.data_ptr(), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
-                                         dcodes_u[i % n_rot].data_ptr(), dscales_u.data_ptr(), wl.M, wl.K,
-                                         wl.N, wl.k, wl.L, wl.T, outs[0].data_ptr(), outs[1].data_ptr(),
-                                         outs[2].data_ptr(), ws.data_ptr(), ws.numel(), s_handle)
-            if rc != 0:
-                raise RuntimeError(f"trellis_gemm_gateup failed: {binding.status_string(rc)}")
-    elif args.entry == "packed":
-        # the workload's M rows as `groups` sequences (sizes as equal as possible),
-        # gathered, multiplied once and scattered back by trellis_gemm_packed
-        rows = group_rows(wl.M, args.groups)
-        offs = np.cumsum([0] + rows)
-        out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
-        xp = (ctypes.c_void_p * len(rows))(*[dx[a:b].data_ptr() for a, b in zip(offs[:-1], offs[1:])])
-        op = (ctypes.c_void_p * len(rows))(*[out[a:b].data_ptr() for a, b in zip(offs[:-1], offs[1:])])
-        rp = (ctypes.c_int * len(rows))(*rows)
-        ws_bytes = binding.gemm_packed_workspace_bytes(rows, wl.K, wl.N, wl.k, wl.L)
-        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
-
-        def call(i):
-            rc = lib.trellis_gemm_packed(xp, rp, len(rows), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
-                                         wl.K, wl.N, wl.k, wl.L, wl.T, op, ws.data_ptr(), ws.numel(), s_handle)
-            if rc != 0:
-                raise RuntimeError(f"trellis_gemm_packed failed: {binding.status_string(rc)}")
-    elif args.entry == "gemm":
-        out = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
-        ws_bytes = binding.gemm_workspace_bytes(wl.M, wl.K, wl.N, wl.k, wl.L)
-        ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
-
-        def call(i):
-            rc = lib.trellis_gemm_ws(dx.data_ptr(), dcodes[i % n_rot].data_ptr(), dscales.data_ptr(),
-                                     wl.M, wl.K, wl.N, wl.k, wl.L, wl.T, out.data_ptr(),
-                                     ws.data_ptr(), ws.numel(), s_handle)
-            if rc != 0:
-                raise RuntimeError(f"trellis_gemm_ws failed: {binding.status_string(rc)}")
-    else:
-        wout = torch.empty((wl.N, wl.K), dtype=torch.bfloat16, device="cuda")
-
-        def call(i):
-            rc = lib.trellis_decode(dcodes[i % n_rot].data_ptr(), dscales.data_ptr(), wl.K, wl.N, wl.k,
-                                    wl.L, wl.T, wout.data_ptr(), s_handle)
-            if rc != 0:
-                raise RuntimeError(f"trellis_decode failed: {binding.status_string(rc)}")
+    ent = Entry(wl, args.entry, lib, torch, stream, args.groups)
+    x, codes, scales = ent.x, ent.codes, ent.scales
     torch.cuda.synchronize()
-
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            call(i)
-    torch.cuda.synchronize()
-
-    # The K steps run back to back on one stream (as a model issues its
-    # layers), bracketed by one pair of events; each step is one launch, so
-    # the average launch duration is the step time.
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.15)
-    if world > 1:
-        dist.barrier()
-    graph = None
-    if args.graph:
-        # the K steps captured once into a CUDA graph (outside the timed region)
-        # and replayed inside it: the same launches, no host launch overhead
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(args.steps):
-                call(args.warmup + i)
-        torch.cuda.synchronize()
-    torch.cuda.synchronize()
-    t_host0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            for i in range(args.steps):
-                call(args.warmup + i)
-        t_end.record(stream)
-    torch.cuda.synchronize()
-    t_host = time.perf_counter() - t_host0
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    ms_step = total_ms / args.steps
+    ms_step, clocks, t_host = time_steps(ent, args.steps, args.warmup, stream, torch, world, local, args.graph)
     kernel_ms = ms_step
 
     # For context, outside the timed region: one call at a time, each between
@@ -377,11 +549,12 @@ def run_ours(args, wl):
     with torch.cuda.stream(stream):
         for i, (a, b) in enumerate(iso):
             a.record(stream)
-            call(args.warmup + args.steps + i)
+            ent.call(args.warmup + args.steps + i)
             b.record(stream)
     torch.cuda.synchronize()
     isolated_ms = statistics.median([a.elapsed_time(b) for a, b in iso])
     ms_step, kernel_ms, isolated_ms = max_over_ranks([ms_step, kernel_ms, isolated_ms], device="cuda")
+    n_mats = ent.n_mats
 
     # ---- end to end through the public API, host buffers in pinned memory ----
     # Every step uploads its inputs from pinned host memory and reads its result
@@ -403,16 +576,18 @@ def run_ours(args, wl):
         if args.entry == "packed":
             from trellis_quantized_weight_gb300 import gemm_packed as tq_packed
             ypk = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+            offs = ent.offs
         if args.entry == "gateup":
             from trellis_quantized_weight_gb300 import gemm_gateup as tq_gateup
-            hcu = torch.from_numpy(codes_u.view(np.int32)).pin_memory()
-            hsu = torch.from_numpy(scales_u.view(np.int16)).view(torch.bfloat16).pin_memory()
+            hcu = torch.from_numpy(ent.codes_u.view(np.int32)).pin_memory()
+            hsu = torch.from_numpy(ent.scales_u.view(np.int16)).view(torch.bfloat16).pin_memory()
         bufs = []
         for _ in range(2):
-            b = {"x": torch.empty_like(dx), "c": torch.empty_like(dcodes[0]), "s": torch.empty_like(dscales)}
+            b = {"x": torch.empty_like(ent.dx), "c": torch.empty_like(ent.dcodes[0]),
+                 "s": torch.empty_like(ent.dscales)}
             if hcu is not None:
-                b["cu"] = torch.empty_like(dcodes[0])
-                b["su"] = torch.empty_like(dscales)
+                b["cu"] = torch.empty_like(ent.dcodes[0])
+                b["su"] = torch.empty_like(ent.dscales)
             bufs.append(b)
         copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]
         free = [None, None]            # event: the product that read set b has finished
@@ -487,77 +662,46 @@ def run_ours(args, wl):
                "d2h_bytes_per_step": hout.numel() * 2,
                "pipelining": "two buffer sets: step i+1's uploads overlap step i's product"}
 
-    # ---- roofline of the step's only kernel ----
-    peaks, peak_src = measured_peaks()
-    sm_max = float(peaks.get("sm_max_mhz") or 2070.0)
-    hbm_peak = float(peaks["hbm_gbs"])
-    alu_peak = props.multi_processor_count * ALU_LANES_PER_SM * sm_max * 1e6 / 1e12   # Tops/s
-    t_kernel = kernel_ms * 1e-3
-    flops = 0
-    tensor_peak = float(peaks.get("bf16_tflops") or 1900.0)
-    if args.entry in ("gemm", "gateup", "packed") and wl.M > 16:
-        # tensor-core path: the decode runs on the ALUs, the M FMAs per weight
-        # are a dense bf16 contraction on the tensor cores
-        ops = n_mats * wl.weights * DECODE_OPS_PER_WEIGHT
-        flops = n_mats * 2 * wl.M * wl.N * wl.K
-        hbm_bytes = n_mats * (wl.code_bytes + wl.M * wl.N * 2) + wl.M * wl.K * 2
-        kernel_name = "gemm_tc"
-    elif args.entry in ("gemm", "gateup", "packed"):
-        # gate/up: both matrices in one launch, plus the elementwise activation
-        # (read 2 and write 1 bf16 [M, N]; bytes counted, no ALU ops)
-        ops = n_mats * wl.weights * (DECODE_OPS_PER_WEIGHT + wl.M)
-        hbm_bytes = n_mats * (wl.code_bytes + wl.M * wl.N * 2) + wl.M * wl.K * 2
-        if args.entry == "gateup":
-            hbm_bytes += 3 * wl.M * wl.N * 2
-        kernel_name = "gemm_smallm"
-    else:
-        ops = wl.weights * DECODE_OPS_PER_WEIGHT
-        hbm_bytes = wl.code_bytes + wl.weights * 2
-        kernel_name = "decode"
-    alu_achieved = ops / t_kernel / 1e12
-    hbm_achieved = hbm_bytes / t_kernel / 1e9
-    tensor_achieved = flops / t_kernel / 1e12
-    t_roof = {"alu": ops / (alu_peak * 1e12), "hbm": hbm_bytes / (hbm_peak * 1e9),
-              "tensor": flops / (tensor_peak * 1e12)}
-    bound = max(t_roof, key=t_roof.get)
-    achieved = {"alu": alu_achieved, "hbm": hbm_achieved, "tensor": tensor_achieved}[bound]
-    peak = {"alu": alu_peak, "hbm": hbm_peak, "tensor": tensor_peak}[bound]
-    t_roof_alu, t_roof_hbm = t_roof["alu"], t_roof["hbm"]
-    roof = {"bound": bound,
-            "achieved": round(achieved, 3),
-            "peak": round(peak, 3),
-            "unit": {"alu": "Tops/s", "hbm": "GB/s", "tensor": "TFLOP/s"}[bound],
-            "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(kernel_name, wl.name),
-            "peak_source": {"alu": f"{peak_src}: {props.multi_processor_count} SMs x {ALU_LANES_PER_SM} lanes x "
-                                   f"{sm_max:.0f} MHz (of measured max clock)",
-                            "hbm": f"{peak_src} hbm_gbs (of measured)",
-                            "tensor": f"{peak_src} bf16_tflops (of measured)"}[bound],
-            "tensor_TFLOPs": round(tensor_achieved, 1) if flops else None,
-            "ops_per_launch": ops, "algorithmic_bytes_per_launch": hbm_bytes,
-            "hbm_GBps": round(hbm_achieved, 1),
-            "hbm_frac": round(hbm_achieved / hbm_peak, 4),
-            "alu_frac": round(alu_achieved / alu_peak, 4),
-            "roofline_us": round(max(t_roof.values()) * 1e6, 2),
-            "kernel_us": round(kernel_ms * 1e3, 2)}
+    roof = roofline(wl, args.entry, kernel_ms, props.multi_processor_count)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        threads = os.cpu_count() or 1
-        gbs, rows, dt = oracle_throughput(wl, x, codes, scales, args.cpu_budget, threads)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{rows} rows x K={wl.K} of {wl.name} (decode + product), {dt:.1f} s wall"}
+        cpu = cpu_baseline_for(wl, x, codes, scales, args.cpu_budget, decode_only=args.entry == "decode")
+
+    config = ent.config(world, args.graph)
+
+    # ---- every configuration, each in its own timed region ----
+    per_config = None
+    if not args.no_per_config:
+        del ent
+        torch.cuda.empty_cache()
+        per_config = {}
+        for name, entry in PER_CONFIG:
+            pwl = synth.WORKLOADS[name]
+            pe = Entry(pwl, entry, lib, torch, stream)
+            torch.cuda.synchronize()
+            p_ms, p_clocks, _ = time_steps(pe, args.per_config_steps, max(3, min(args.warmup, 20)), stream,
+                                           torch, world, local)
+            (p_ms,) = max_over_ranks([p_ms], device="cuda")
+            r = roofline(pwl, entry, p_ms, props.multi_processor_count)
+            key = name if entry == "gemm" else f"decode_k{pwl.K}_n{pwl.N}_k{pwl.k}"
+            per_config[key] = {
+                "entry": "trellis_" + entry, "M": pwl.M, "K": pwl.K, "N": pwl.N, "k": pwl.k,
+                "us_per_call": round(p_ms * 1e3, 2),
+                "value": round(whole_job_gbs(world, pwl.code_bytes, p_ms), 2), "unit": "GB/s",
+                "roofline": {kk: r[kk] for kk in ("bound", "frac", "roofline_us", "achieved", "peak", "unit",
+                                                  "hbm_frac", "alu_frac", "traffic")},
+                "steps": args.per_config_steps, "clocks": p_clocks,
+                "l2": f"rotating {pe.n_rot} code copies",
+            }
+            if rank == 0 and not args.no_cpu_baseline:
+                per_config[key]["cpu_baseline"] = cpu_baseline_for(pwl, pe.x, pe.codes, pe.scales,
+                                                                   args.cpu_budget_per_config,
+                                                                   decode_only=entry == "decode")
+            del pe
+            torch.cuda.empty_cache()
 
     value = whole_job_gbs(world, n_mats * wl.code_bytes, ms_step)
-    # our kernels per step: on the tensor cores one launch per matrix for M <= 256,
-    # else one per 256-row chunk; otherwise one small-M launch; plus the gate/up
-    # activation
-    chunks = max(1, (wl.M + 255) // 256) if wl.M > 16 and args.entry != "decode" else 1
-    launches_per_step = n_mats * chunks if wl.M > 16 and args.entry != "decode" else 1
-    if args.entry == "gateup":
-        launches_per_step += 1
-    if args.entry == "packed" and args.groups > 1:   # the gather and the scatter, per 64 groups
-        launches_per_step += 2 * ((args.groups + 63) // 64)
     line = {
         "metric": {"gemm": METRIC, "decode": METRIC_DECODE, "gateup": METRIC_GATEUP,
                    "packed": METRIC_PACKED}[args.entry],
@@ -567,13 +711,11 @@ def run_ours(args, wl):
         "us_per_call": round(ms_step * 1e3, 2), "isolated_call_us": round(isolated_ms * 1e3, 2),
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": path_dtype(args.entry, wl.M), "data": "synthetic",
-        "config": {"workload": wl.name, "entry": "trellis_" + args.entry, "M": wl.M, "K": wl.K, "N": wl.N,
-                   **({"groups": group_rows(wl.M, args.groups)} if args.entry == "packed" else {}),
-                   "k": wl.k, "L": wl.L, "T": wl.T, "parallelism": f"replicas{world}",
-                   "launch": "CUDA graph of the K steps" if args.graph else "stream, programmatic launches",
-                   "l2": f"rotating {n_rot} code copies ({n_rot * wl.code_bytes / 1e6:.0f} MB > 2x L2)"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
+        "config": config,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": args.steps * launches_per_step(args.entry, wl.M, args.groups),
         "clocks": clocks, "host_wall_s": round(t_host, 3),
+        "per_config": per_config,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -587,7 +729,7 @@ def run_reference(args, wl):
     if rank != 0:
         return
     x, codes, scales = wl.generate()
-    threads = os.cpu_count() or 1
+    threads = len(host_cores())
     # size each step so that warm-up + steps take about args.ref_budget seconds
     per_step = max(0.002, args.ref_budget / max(1, args.steps + args.warmup))
     import oracle
@@ -626,7 +768,8 @@ def run_reference(args, wl):
         "config": {"workload": wl.name, "M": wl.M, "K": wl.K, "N": wl.N, "k": wl.k, "L": wl.L, "T": wl.T,
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{rows} rows x K={wl.K} per step (decode + product)"},
+                         "sample": f"{rows} rows x K={wl.K} per step (decode + product)",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -648,7 +791,12 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=5.0,
+                    help="seconds of oracle work for cpu_baseline (each of all cores and one core)")
+    ap.add_argument("--cpu-budget-per-config", type=float, default=1.0,
+                    help="seconds of oracle work per configuration (each of all cores and one core)")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-configuration table")
+    ap.add_argument("--per-config-steps", type=int, default=2000)
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds for the reference arm's timed run")
     ap.add_argument("--rows", type=int, default=None,
                     help="activation rows M instead of the workload's own (a prefill sweep of the same weights)")
