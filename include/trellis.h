@@ -172,7 +172,12 @@ int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *sc
  * device-side wait of the tensor-core product gave up since the last query
  * (TRELLIS_ERR_TIMEOUT; the affected outputs are undefined) or not
  * (TRELLIS_OK).  Clears the flag.  A wait gives up after 2 s of wall-clock
- * time; the kernel then winds down and returns, so the context stays usable.
+ * time; the kernel then waits (bounded the same way) for its own copies and
+ * tensor-core operations still in flight, releases its tensor memory and
+ * returns, so the context stays usable.  The flag is one word per device,
+ * shared by every stream and every caller on that device: a timeout on any
+ * stream is reported to, and cleared by, whichever query comes first, and
+ * synchronising `stream` does not wait for work on other streams.
  * No counterpart on the pages: it is how the library surfaces its own wait
  * limits.
  */

@@ -33,7 +33,11 @@
 // to bf16 and store out[m, n] (each store instruction writes 32 consecutive n).
 //
 // Every mbarrier wait is bounded; a wait that runs out records an error in a
-// device word (read by trellis_device_status) and the CTA winds down.
+// device word (read by trellis_device_status) and the CTA winds down without
+// leaving asynchronous work behind: the activation copies complete on
+// barriers of their own, which the TMA thread waits for (bounded) before it
+// leaves, and the MMA thread always commits and waits for its last MMAs, so
+// nothing is in flight when the tensor memory is released.
 #include <cuda.h>
 #include <cstdint>
 #include <mutex>
@@ -81,8 +85,8 @@ struct TcShape {
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
     static constexpr int kOffBar = kOffB + kStages * kBBytes;
-    static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarDone = 2 * kStages;
-    static constexpr int kOffTaddr = kOffBar + (2 * kStages + 1) * 8;
+    static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarTma = 2 * kStages, kBarDone = 3 * kStages;
+    static constexpr int kOffTaddr = kOffBar + (3 * kStages + 1) * 8;
     // + 1 KB so that the base can be rounded up to the 1 KB the swizzle atoms need
     static constexpr int kSmemBytes = kOffTaddr + 16 + 1024;
     static constexpr int kTmemCols = NB;   // fp32 accumulator: 128 lanes x NB columns
@@ -201,6 +205,7 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
     constexpr int kBBytes = S::kBBytes;
     constexpr int kOffA = S::kOffA, kOffB = S::kOffB, kOffBar = S::kOffBar, kOffTaddr = S::kOffTaddr;
     constexpr int kBarFull = S::kBarFull, kBarEmpty = S::kBarEmpty, kBarDone = S::kBarDone;
+    constexpr int kBarTma = S::kBarTma;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sraw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
@@ -209,13 +214,15 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
     const uint32_t bar_full = sbase + kOffBar + 8 * kBarFull;
     const uint32_t bar_empty = sbase + kOffBar + 8 * kBarEmpty;
     const uint32_t bar_done = sbase + kOffBar + 8 * kBarDone;
+    const uint32_t bar_tma = sbase + kOffBar + 8 * kBarTma;
     const int nstages = K / kTcStageK;
     const int n0 = blockIdx.x * kTcRows;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(bar_full + 8 * s, kTcDecodeWarps + 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, kTcDecodeWarps);   // one arrival per decode warp
+            mbar_init(bar_empty + 8 * s, 1);               // the MMAs' commit
+            mbar_init(bar_tma + 8 * s, 1);                 // the TMA thread's expect_tx, then the bytes
         }
         mbar_init(bar_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -345,24 +352,32 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
             // one box per k-block: the chunk's rows rounded up to 8 (rows past
             // M zero-filled by the TMA) x 64 k, 128 bytes a row
             const int rows = tc_box_rows(M, NB);
+            int issued = 0;
             for (int i = 0; i < nstages; ++i) {
                 const int s = i % kTcStages;
                 if (i >= kTcStages && !mbar_wait(bar_empty + 8 * s, ((i / kTcStages) + 1) & 1)) break;
-                mbar_arrive_expect_tx(bar_full + 8 * s, static_cast<uint32_t>(2 * rows * kSwRowBytes));
+                mbar_arrive_expect_tx(bar_tma + 8 * s, static_cast<uint32_t>(2 * rows * kSwRowBytes));
                 const uint32_t dst = sbase + kOffB + s * kBBytes;
 #pragma unroll
                 for (int kb = 0; kb < kTcStageK / kSwK; ++kb)
                     tma_load_2d(dst + kb * (NB * kSwRowBytes), &x_map, i * kTcStageK + kb * kSwK, 0,
-                                bar_full + 8 * s);
+                                bar_tma + 8 * s);
+                issued = i + 1;
             }
+            // Before the CTA can exit, every copy it issued has landed.  The
+            // copies of the last (up to) kTcStages issued stages may not have
+            // been consumed yet, but their completion depends on nothing else:
+            // wait (bounded) for each.  After a normal run these return at once.
+            for (int i = issued > kTcStages ? issued - kTcStages : 0; i < issued; ++i)
+                (void)mbar_wait(bar_tma + 8 * (i % kTcStages), (i / kTcStages) & 1);
         }
     } else {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            bool ok = true;
             for (int i = 0; i < nstages; ++i) {
                 const int s = i % kTcStages;
-                if (!mbar_wait(bar_full + 8 * s, (i / kTcStages) & 1)) { ok = false; break; }
+                if (!mbar_wait(bar_full + 8 * s, (i / kTcStages) & 1)) break;
+                if (!mbar_wait(bar_tma + 8 * s, (i / kTcStages) & 1)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t a0 = sbase + kOffA + s * kABytes;
                 const uint32_t b0 = sbase + kOffB + s * kBBytes;
@@ -375,8 +390,11 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                 }
                 mma_commit(bar_empty + 8 * s);
             }
-            mma_commit(bar_done);   // tracks every MMA issued above
-            (void)ok;
+            // tracks every MMA issued above; also waited for here, so that no
+            // MMA is in flight when the tensor memory is released, whether the
+            // loop ran to the end or gave up
+            mma_commit(bar_done);
+            (void)mbar_wait(bar_done, 0);
         }
     }
 
