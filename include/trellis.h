@@ -51,6 +51,15 @@
 extern "C" {
 #endif
 
+/* The library exports exactly the functions below; everything else in it has
+ * hidden visibility (so that two copies of the library in one process never
+ * share internal state). */
+#if defined(__GNUC__) || defined(__clang__)
+#define TRELLIS_API __attribute__((visibility("default")))
+#else
+#define TRELLIS_API
+#endif
+
 /* The CUDA runtime's stream handle, declared the way the runtime declares it,
  * so that this header does not need the CUDA headers. */
 struct CUstream_st;
@@ -70,10 +79,10 @@ typedef enum trellis_status {
 } trellis_status;
 
 /* ABI version compiled into the library (TRELLIS_ABI_VERSION). */
-int trellis_abi_version(void);
+TRELLIS_API int trellis_abi_version(void);
 
 /* Human-readable name of a status code; never NULL, static storage. */
-const char *trellis_status_string(int status);
+TRELLIS_API const char *trellis_status_string(int status);
 
 /*
  * trellis_decode — expand packed codes into the dense bf16 weight matrix
@@ -91,8 +100,8 @@ const char *trellis_status_string(int status);
  * K <= 0, N <= 0, K % T != 0 or N*K too large -> TRELLIS_ERR_SHAPE;
  * k, L or T outside the accepted set -> TRELLIS_ERR_UNSUPPORTED.
  */
-int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, int k, int L,
-                   int T, uint16_t *out_bf16, cudaStream_t stream);
+TRELLIS_API int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, int k, int L,
+                               int T, uint16_t *out_bf16, cudaStream_t stream);
 
 /*
  * trellis_gemm — fused decode-and-multiply out[m, n] = sum_k w[n, k] * x[m, k]
@@ -135,15 +144,15 @@ int trellis_decode(const uint32_t *codes, const uint16_t *scales, int K, int N, 
  * on a device with more than 256 SMs the region is too small for M <= 16 ->
  * TRELLIS_ERR_WORKSPACE (use trellis_gemm_ws).
  */
-int trellis_gemm(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M, int K,
-                 int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
+TRELLIS_API int trellis_gemm(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M, int K,
+                             int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
 
 /*
  * trellis_gemm_workspace_size — bytes of workspace trellis_gemm_ws needs for
  * this geometry on the CURRENT device (it depends on the SM count).
  * Writes the size to *bytes.  Same validation as trellis_gemm.
  */
-int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t *bytes);
+TRELLIS_API int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t *bytes);
 
 /*
  * trellis_gemm_ws — trellis_gemm with a caller-owned workspace.
@@ -163,9 +172,9 @@ int trellis_gemm_workspace_size(int M, int K, int N, int k, int L, int T, size_t
  * Errors: as trellis_gemm, plus TRELLIS_ERR_WORKSPACE when the workspace is
  * NULL or too small, TRELLIS_ERR_ALIGN when it is misaligned.
  */
-int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
-                    int K, int N, int k, int L, int T, uint16_t *out, void *workspace,
-                    size_t workspace_bytes, cudaStream_t stream);
+TRELLIS_API int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
+                                int K, int N, int k, int L, int T, uint16_t *out, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * trellis_device_status — synchronise `stream`, then report whether a bounded
@@ -181,7 +190,7 @@ int trellis_gemm_ws(const uint16_t *x, const uint32_t *codes, const uint16_t *sc
  * No counterpart on the pages: it is how the library surfaces its own wait
  * limits.
  */
-int trellis_device_status(cudaStream_t stream);
+TRELLIS_API int trellis_device_status(cudaStream_t stream);
 
 /*
  * trellis_selftest_wait_timeout — enqueue on `stream` a one-thread kernel
@@ -191,7 +200,7 @@ int trellis_device_status(cudaStream_t stream);
  * reporting path without a hang or a fault.  Returns TRELLIS_OK or
  * TRELLIS_ERR_CUDA.
  */
-int trellis_selftest_wait_timeout(cudaStream_t stream);
+TRELLIS_API int trellis_selftest_wait_timeout(cudaStream_t stream);
 
 /*
  * trellis_gemm_gateup — the two projections of a gated MLP that share x, in
@@ -216,16 +225,16 @@ int trellis_selftest_wait_timeout(cudaStream_t stream);
  * Errors: as trellis_gemm_ws for either matrix; out_act misaligned ->
  * TRELLIS_ERR_ALIGN.
  */
-int trellis_gemm_gateup(const uint16_t *x, const uint32_t *codes_gate, const uint16_t *scales_gate,
-                        const uint32_t *codes_up, const uint16_t *scales_up, int M, int K, int N, int k,
-                        int L, int T, uint16_t *out_gate, uint16_t *out_up, uint16_t *out_act,
-                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
+TRELLIS_API int trellis_gemm_gateup(const uint16_t *x, const uint32_t *codes_gate, const uint16_t *scales_gate,
+                                    const uint32_t *codes_up, const uint16_t *scales_up, int M, int K, int N, int k,
+                                    int L, int T, uint16_t *out_gate, uint16_t *out_up, uint16_t *out_act,
+                                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * trellis_gemm_gateup_workspace_size — bytes of workspace trellis_gemm_gateup
  * needs on the current device.  Same validation as trellis_gemm.
  */
-int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T, size_t *bytes);
+TRELLIS_API int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T, size_t *bytes);
 
 /*
  * trellis_gemm_noalloc — trellis_gemm for callers that cannot allocate device
@@ -255,8 +264,8 @@ int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, int L, int T,
  * TRELLIS_ERR_WORKSPACE before any launch (a guard for devices with more than
  * 1280 SMs: below that the scratch of every accepted geometry fits).
  */
-int trellis_gemm_noalloc(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
-                         int K, int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
+TRELLIS_API int trellis_gemm_noalloc(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
+                                     int K, int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
 
 /*
  * trellis_gemm_packed — token packing: several independent groups of
@@ -289,17 +298,17 @@ int trellis_gemm_noalloc(const uint16_t *x, const uint32_t *codes, const uint16_
  * TRELLIS_ERR_UNSUPPORTED; the rest as trellis_gemm_ws.  All checks run before
  * anything is enqueued.
  */
-int trellis_gemm_packed(const uint16_t *const *xs, const int *rows, int groups, const uint32_t *codes,
-                        const uint16_t *scales, int K, int N, int k, int L, int T, uint16_t *const *outs,
-                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
+TRELLIS_API int trellis_gemm_packed(const uint16_t *const *xs, const int *rows, int groups, const uint32_t *codes,
+                                    const uint16_t *scales, int K, int N, int k, int L, int T, uint16_t *const *outs,
+                                    void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * trellis_gemm_packed_workspace_size — bytes of workspace trellis_gemm_packed
  * needs for these groups on the current device.  Same validation as
  * trellis_gemm_packed for the sizes.
  */
-int trellis_gemm_packed_workspace_size(const int *rows, int groups, int K, int N, int k, int L, int T,
-                                       size_t *bytes);
+TRELLIS_API int trellis_gemm_packed_workspace_size(const int *rows, int groups, int K, int N, int k, int L, int T,
+                                                   size_t *bytes);
 
 #ifdef __cplusplus
 }

@@ -29,6 +29,22 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), n
 
 
+def test_library_exports_only_the_declared_functions(lib):
+    """Everything but the C ABI has hidden visibility: no internal symbol (in
+    particular no template-local static, which the dynamic linker would merge
+    across two copies of the library loaded into one process) is exported."""
+    import shutil
+    import subprocess
+    from trellis_quantized_weight_gb300 import build
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm is not installed")
+    out = subprocess.run([nm, "-D", "--defined-only", build.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert exported == set(declared_functions())
+
+
 def test_binding_signatures_cover_header(lib):
     from trellis_quantized_weight_gb300 import binding
     assert set(declared_functions()) == set(binding.SIGNATURES)

@@ -68,6 +68,19 @@ def test_gemm_general_geometry(tq, oracle_lib, k, L, M):
     assert_gemm_close(bits[: M * N].reshape(M, N), ref, refabs, f"M={M} k={k} L={L}")
 
 
+@pytest.mark.parametrize("k,L,M", [(8, 16, 15), (4, 16, 16), (6, 20, 16), (7, 12, 16), (8, 9, 14)])
+def test_gemm_general_two_row_shapes(tq, oracle_lib, k, L, M):
+    """The general-geometry shapes with two rows a lane (M = 15 at k = 8; M = 16
+    at k = 4, 6, 7), next to a three-row one, on several tile-groups, a ragged N
+    and K-ranges split over CTAs."""
+    N, K = 1001, 2048
+    x, codes, scales = _inputs(M, K, N, k, seed=9000 + 17 * M + k + L)
+    got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), k, L=L))
+    w = oracle_decode_par(oracle_lib, codes, scales, K, N, k, L=L)
+    ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+    assert_gemm_close(got, ref, refabs, f"M={M} k={k} L={L}")
+
+
 @pytest.mark.parametrize("k,L,M", [(1, 24, 16), (5, 16, 9), (8, 10, 40), (7, 12, 256)])
 def test_gemm_general_one_hot_rows_are_exact(tq, oracle_lib, k, L, M):
     """Row i of x selects weight column j_i: each output row is that decoded

@@ -553,3 +553,29 @@ def test_cuda_graph_capture_replays_the_eager_bits(tq, M, K, N, k):
         torch.cuda.synchronize()
         assert np.array_equal(out.view(torch.int16).cpu().numpy(), want)
     assert lib.trellis_device_status(None) == 0
+
+
+def test_two_copies_of_the_library_in_one_process(tq, tmp_path):
+    """A second copy of the library (another file, as when two versions are
+    loaded into one process) keeps its own per-device state: both copies
+    launch the shared-memory-heavy small-M kernel and give the same bits."""
+    import shutil
+    import torch
+    from trellis_quantized_weight_gb300 import binding, build
+    copy_path = str(tmp_path / "libtrellis_copy.so")
+    shutil.copy(build.LIB_PATH, copy_path)
+    libs = [binding.load(), ctypes.CDLL(copy_path)]
+    M, K, N, k = 15, 1024, 1000, 4
+    x, codes, scales = _inputs(M, K, N, k, seed=4711)
+    dx, dc, ds = dev_bf16(x), dev_codes(codes), dev_bf16(scales)
+    s = torch.cuda.current_stream().cuda_stream
+    outs = []
+    for lib in libs:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        rc = lib.trellis_gemm(ctypes.c_void_p(dx.data_ptr()), ctypes.c_void_p(dc.data_ptr()),
+                              ctypes.c_void_p(ds.data_ptr()), M, K, N, k, 12, 256, ctypes.c_void_p(out.data_ptr()),
+                              ctypes.c_void_p(s))
+        assert rc == 0, binding.status_string(rc)
+        outs.append(host_bits(out))
+    torch.cuda.synchronize()
+    assert np.array_equal(outs[0], outs[1])

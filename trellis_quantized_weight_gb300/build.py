@@ -21,7 +21,10 @@ LIB_NAME = "libtrellis_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
+# Host code with hidden visibility: the library exports only the C ABI (marked
+# in include/trellis.h), so its internal statics stay private to each copy.
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
+              "--expt-relaxed-constexpr"]
 
 
 def cuda_home() -> str:

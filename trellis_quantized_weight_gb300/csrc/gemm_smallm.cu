@@ -7,18 +7,25 @@
 namespace trellis {
 
 // 0 when the geometry needs more tile counters than the workspace layout holds.
+template <class C>
+static size_t ws_bytes_of(int K, int N, int k, const DeviceInfo& dev, bool two) {
+    const SmallMPlan p = plan_smallm<C>(K, N, k, dev, two);
+    return smallm_fits_counters<C>(p) ? smallm_workspace_bytes<C>(p) : 0;
+}
+
 template <int MM>
 static size_t ws_bytes_for(int K, int N, int k, int L, const DeviceInfo& dev, bool two) {
-    if (fast_geometry(k, L)) {
-        using C = typename SmallMDefault<MM>::type;
-        const SmallMPlan p = plan_smallm<C>(K, N, k, dev, two);
-        return smallm_fits_counters<C>(p) ? smallm_workspace_bytes<C>(p) : 0;
-    }
+    if (fast_geometry(k, L)) return ws_bytes_of<typename SmallMDefault<MM>::type>(K, N, k, dev, two);
     // other geometries run the two matrices of a pair as two launches, one
     // after the other on the stream, through the same workspace
-    using C = typename SmallMDefault<MM>::general;
-    const SmallMPlan p = plan_smallm<C>(K, N, k, dev, false);
-    return smallm_fits_counters<C>(p) ? smallm_workspace_bytes<C>(p) : 0;
+    switch (k) {
+#define TRELLIS_GK(KV) \
+    case KV: return ws_bytes_of<typename SmallMDefault<MM>::template general<KV>>(K, N, k, dev, false);
+        TRELLIS_GK(1) TRELLIS_GK(2) TRELLIS_GK(3) TRELLIS_GK(4)
+        TRELLIS_GK(5) TRELLIS_GK(6) TRELLIS_GK(7) TRELLIS_GK(8)
+#undef TRELLIS_GK
+        default: return 0;
+    }
 }
 
 size_t gemm_smallm_workspace_bytes(int M, int K, int N, int k, int L, const DeviceInfo& dev, bool two) {

@@ -11,7 +11,7 @@ int launch_smallm_g_k<2>(int M, int L, const uint16_t* x, const uint32_t* codes,
                          const DeviceInfo& dev) {
     switch (M) {
 #define TRELLIS_CASE(MV) \
-    case MV: return launch_smallm_instance<typename SmallMDefault<MV>::general, 2, 0>(x, codes, scales, K, N, out, ws, ws_bytes, stream, dev, SecondMatrix{}, L);
+    case MV: return launch_smallm_instance<typename SmallMDefault<MV>::template general<2>, 2, 0>(x, codes, scales, K, N, out, ws, ws_bytes, stream, dev, SecondMatrix{}, L);
         TRELLIS_CASE(1) TRELLIS_CASE(2) TRELLIS_CASE(3) TRELLIS_CASE(4)
         TRELLIS_CASE(5) TRELLIS_CASE(6) TRELLIS_CASE(7) TRELLIS_CASE(8)
         TRELLIS_CASE(9) TRELLIS_CASE(10) TRELLIS_CASE(11) TRELLIS_CASE(12)

@@ -131,9 +131,16 @@ struct SmallMDefault {
     using two = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, true>;   // gate and up
     // any other (k, L): the quotient table only holds the byte sums that
     // 12-bit windows reach, so these compute the quotient, which needs more
-    // registers: 8 warps (255 registers a thread) from M = 6 up
+    // registers: 8 warps (255 registers a thread) from M = 6 up, and 2 rows a
+    // lane where 3 spill heavily at k words a group and measured slower
+    // (M = 15 with k = 8; M = 16 with k = 4, 6, 7; A/B on one GB300 at
+    // K = 5120, N = 17408)
     static constexpr int GWARPS = (MM <= 2) ? 16 : (MM <= 5 ? 12 : 8);
-    using general = SmallMCfg<MM, 3, GWARPS, false, 1, UB, GM, ET>;
+    static constexpr int general_rows(int kb) {
+        return ((MM == 15 && kb == 8) || (MM == 16 && (kb == 4 || kb == 6 || kb == 7))) ? 2 : 3;
+    }
+    template <int KB>
+    using general = SmallMCfg<MM, general_rows(KB), GWARPS, false, 1, UB, GM, ET>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
 
