@@ -175,21 +175,22 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  :: "r"(bar) : "memory");
 }
 
-// Group 4*(stage%2) + gi of block stage/2 of a row, and its lookahead word
-// (only the gi == 0 lanes need one from memory: groups 0 and 4 take it from
-// the other half block, the others from the neighbouring lane).
+// The k words of group 4*(stage%2) + gi of block stage/2 of a row (zeros for
+// a row past N).  The window tails of the group spill into one more word; for
+// gi = 1..3 that is the neighbouring lane's first word, and for groups 0 and 4
+// (gi = 0) it is the first word of group 7 or 3 of the same block, which the
+// gi = 3 lane of the same row loads for the other stage of the block: both
+// arrive by shuffles (a second load here would double the loads in flight).
 template <int KB>
 __device__ __forceinline__ void tc_load_group(const uint32_t* __restrict__ row_codes, bool ok, int stage,
-                                              int gi, uint32_t (&w)[KB], uint32_t& extra) {
+                                              int gi, uint32_t (&w)[KB]) {
     constexpr int WPB = kGroupsPerBlock * KB;
     const int b = stage >> 1, g = 4 * (stage & 1) + gi;
     if (ok) {
         ldg_group<KB>(row_codes + b * WPB + (kGroupsPerBlock - 1 - g) * KB, w);
-        extra = (gi == 0) ? __ldg(row_codes + b * WPB + ((kGroupsPerBlock - g) * KB) % WPB) : 0u;
     } else {
 #pragma unroll
         for (int i = 0; i < KB; ++i) w[i] = 0u;
-        extra = 0u;
     }
 }
 
@@ -250,6 +251,7 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         const float2 s2 = make_float2(sr, sr);
         const uint32_t* row_codes = codes + static_cast<size_t>(ok ? row : 0) * row_words;
         const int src_lane = (gi == 0) ? lane : lane - 8;
+        const int r8 = lane & 7;
         // this thread's 64 bytes (k = 32*gi .. 32*gi+31) inside a stage's A
         // tile: k-block gi/2, 16-byte chunks 4*(gi%2) + q, swizzled by row
         const uint32_t a_row_off = static_cast<uint32_t>((gi >> 1) * kAKBlockBytes + row_local * kSwRowBytes);
@@ -259,18 +261,19 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
         // loaded while stage i is decoded (ring indices are compile-time
         // because the stage loop is unrolled by the ring depth)
         constexpr int D = 4;
-        uint32_t ring[D][KB], ringx[D];
+        static_assert(D % 2 == 0, "stage and ring slot share their parity");
+        uint32_t ring[D][KB];
 #pragma unroll
         for (int d = 0; d < D - 1; ++d) {
             if (d < nstages) {
-                tc_load_group<KB>(row_codes, ok, d, gi, ring[d], ringx[d]);
+                tc_load_group<KB>(row_codes, ok, d, gi, ring[d]);
             } else {
 #pragma unroll
                 for (int q = 0; q < KB; ++q) ring[d][q] = 0u;
-                ringx[d] = 0u;
             }
         }
         bool alive = true;
+        uint32_t carry = 0u;   // word 4k of the block, for the odd stage
         for (int i0 = 0; i0 < nstages && alive; i0 += D) {
 #pragma unroll
             for (int d = 0; d < D; ++d) {
@@ -278,14 +281,24 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                 if (i >= nstages || !alive) break;
                 const int s = i % kTcStages;
                 const int pre = i + D - 1;
-                if (pre < nstages) {
-                    tc_load_group<KB>(row_codes, ok, pre, gi, ring[(d + D - 1) % D], ringx[(d + D - 1) % D]);
-                }
+                if (pre < nstages) tc_load_group<KB>(row_codes, ok, pre, gi, ring[(d + D - 1) % D]);
                 uint32_t w[KB + 1];
 #pragma unroll
                 for (int q = 0; q < KB; ++q) w[q] = ring[d][q];
                 const uint32_t nb = __shfl_sync(0xffffffffu, ring[d][0], src_lane);
-                w[KB] = (gi == 0) ? ringx[d] : nb;
+                // the lookahead word of groups 0 and 4 (the gi == 0 lanes): word
+                // 0 of the block (group 7's first word, loaded for the odd stage
+                // by the gi == 3 lane of the same row and already in the ring),
+                // or word 4k (group 3's first word, handed over during the even
+                // stage; i and d have the same parity because D is even)
+                uint32_t look;
+                if ((d & 1) == 0) {
+                    look = __shfl_sync(0xffffffffu, ring[(d + 1) % D][0], r8 + 24);
+                    carry = __shfl_sync(0xffffffffu, ring[d][0], r8 + 24);
+                } else {
+                    look = carry;
+                }
+                w[KB] = (gi == 0) ? look : nb;
 
                 uint32_t packed[16];
 #pragma unroll
