@@ -387,19 +387,28 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
     } else {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
+            // The descriptors of stage slot 0 at k step 0; every other operand
+            // start is a fixed byte offset from it, a multiple of 16 that adds
+            // to the start-address field (bits 0-13, shared-memory offsets
+            // below 256 KB never carry out of it), so one 32-bit add per MMA
+            // operand replaces rebuilding the descriptor: this thread shares
+            // its sub-partition's issue slots with four decode warps.
+            const uint64_t da0 = smem_desc(sbase + kOffA), db0 = smem_desc(sbase + kOffB);
+            const uint32_t da_hi = static_cast<uint32_t>(da0 >> 32), db_hi = static_cast<uint32_t>(db0 >> 32);
             for (int i = 0; i < nstages; ++i) {
                 const int s = i % kTcStages;
                 if (!mbar_wait(bar_full + 8 * s, (i / kTcStages) & 1)) break;
                 if (!mbar_wait(bar_tma + 8 * s, (i / kTcStages) & 1)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = sbase + kOffA + s * kABytes;
-                const uint32_t b0 = sbase + kOffB + s * kBBytes;
+                const uint32_t da_s = static_cast<uint32_t>(da0) + static_cast<uint32_t>(s * (kABytes >> 4));
+                const uint32_t db_s = static_cast<uint32_t>(db0) + static_cast<uint32_t>(s * (kBBytes >> 4));
 #pragma unroll
                 for (int kk = 0; kk < kTcStageK / 16; ++kk) {
                     const int kb = kk / (kSwK / 16), ks = kk % (kSwK / 16);
-                    mma_bf16(taddr, smem_desc(a0 + kb * kAKBlockBytes + ks * 32),
-                             smem_desc(b0 + kb * (NB * kSwRowBytes) + ks * 32), S::kInstrDesc,
-                             (i > 0 || kk > 0) ? 1u : 0u);
+                    const uint32_t a_lo = da_s + static_cast<uint32_t>((kb * kAKBlockBytes + ks * 32) >> 4);
+                    const uint32_t b_lo = db_s + static_cast<uint32_t>((kb * (NB * kSwRowBytes) + ks * 32) >> 4);
+                    mma_bf16(taddr, (static_cast<uint64_t>(da_hi) << 32) | a_lo,
+                             (static_cast<uint64_t>(db_hi) << 32) | b_lo, S::kInstrDesc, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar_empty + 8 * s);
             }
