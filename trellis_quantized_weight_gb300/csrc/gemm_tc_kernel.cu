@@ -397,8 +397,11 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
             const uint32_t da_hi = static_cast<uint32_t>(da0 >> 32), db_hi = static_cast<uint32_t>(db0 >> 32);
             for (int i = 0; i < nstages; ++i) {
                 const int s = i % kTcStages;
-                if (!mbar_wait(bar_full + 8 * s, (i / kTcStages) & 1)) break;
+                // the activation copy lands long before the decode warps are
+                // done, so its barrier is checked first: only one probe stands
+                // between the last decode arrival and the MMAs
                 if (!mbar_wait(bar_tma + 8 * s, (i / kTcStages) & 1)) break;
+                if (!mbar_wait(bar_full + 8 * s, (i / kTcStages) & 1)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t da_s = static_cast<uint32_t>(da0) + static_cast<uint32_t>(s * (kABytes >> 4));
                 const uint32_t db_s = static_cast<uint32_t>(db0) + static_cast<uint32_t>(s * (kBBytes >> 4));
