@@ -308,7 +308,19 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                     const float2 ws = __fmul2_rn(v, s2);
                     packed[jp] = pack_bf16x2(ws.x, ws.y);
                 }
-                if (i >= kTcStages) alive = mbar_wait(bar_empty + 8 * s, ((i / kTcStages) + 1) & 1);
+                if constexpr (kTcStages == 4) {
+                    // Four slots: an even stage i and the odd stage i + 1 go to
+                    // slots 0/2 and 1/3.  Only the odd stage's slot is probed,
+                    // before the pair's first write: the commit that frees it
+                    // (MMAs of stage i - 3) tracks every earlier MMA, those of
+                    // stage i - 4 included.  Slots 1 and 3 are probed at every
+                    // one of their phases, slots 0 and 2 never, so no probe
+                    // skips a phase of its barrier.
+                    if ((d & 1) == 0 && i + 1 >= kTcStages)
+                        alive = mbar_wait(bar_empty + 8 * ((i + 1) % kTcStages), (((i + 1) / kTcStages) + 1) & 1);
+                } else {
+                    if (i >= kTcStages) alive = mbar_wait(bar_empty + 8 * s, ((i / kTcStages) + 1) & 1);
+                }
                 if (!alive) break;
                 const uint32_t dst = sbase + kOffA + s * kABytes + a_row_off;
 #pragma unroll
