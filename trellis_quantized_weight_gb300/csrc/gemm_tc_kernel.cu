@@ -238,7 +238,24 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t taddr = *reinterpret_cast<volatile uint32_t*>(smem + kOffTaddr);
-    // everything above is on-chip set-up; global memory only after this
+    // Before the wait for the previous grid: L2 prefetches of the code words
+    // of the first stages (no data reaches registers; L2 is where every write
+    // becomes visible, so a line fetched now cannot go stale), so that the
+    // first loads after the wait hit L2.
+    if (warp < kTcDecodeWarps) {
+        const int prow = n0 + warp * 8 + (lane & 7);
+        const int pgi = (lane >> 3) & 3;
+        if (prow < N) {
+            const uint32_t* rc = codes + static_cast<size_t>(prow) * row_words;
+            constexpr int WPB = kGroupsPerBlock * KB;
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+                if (st < nstages)
+                    asm volatile("prefetch.global.L2 [%0];"
+                                 :: "l"(rc + (st >> 1) * WPB + (kGroupsPerBlock - 1 - (4 * (st & 1) + pgi)) * KB));
+        }
+    }
+    // everything above touches no global memory but L2 prefetches; loads only after this
     griddep_wait();
 
     if (warp < kTcDecodeWarps) {
@@ -407,14 +424,15 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
             // its sub-partition's issue slots with four decode warps.
             const uint64_t da0 = smem_desc(sbase + kOffA), db0 = smem_desc(sbase + kOffB);
             const uint32_t da_hi = static_cast<uint32_t>(da0 >> 32), db_hi = static_cast<uint32_t>(db0 >> 32);
-            for (int i = 0; i < nstages; ++i) {
+            // With four slots the decode warps publish stages in pairs (their
+            // arrivals for stages i and i + 1 come together), so the pair is
+            // taken as a unit: the four barrier probes are issued back to back
+            // and their latencies overlap, instead of four in a row between the
+            // last decode arrival and the pair's MMAs (measured slower with
+            // three slots, where it stays one stage at a time).
+            constexpr int P = kTcStages == 4 ? 2 : 1;
+            auto issue_stage = [&](int i) {
                 const int s = i % kTcStages;
-                // the activation copy lands long before the decode warps are
-                // done, so its barrier is checked first: only one probe stands
-                // between the last decode arrival and the MMAs
-                if (!mbar_wait(bar_tma + 8 * s, (i / kTcStages) & 1)) break;
-                if (!mbar_wait(bar_full + 8 * s, (i / kTcStages) & 1)) break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t da_s = static_cast<uint32_t>(da0) + static_cast<uint32_t>(s * (kABytes >> 4));
                 const uint32_t db_s = static_cast<uint32_t>(db0) + static_cast<uint32_t>(s * (kBBytes >> 4));
 #pragma unroll
@@ -426,6 +444,26 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
                              (static_cast<uint64_t>(db_hi) << 32) | b_lo, S::kInstrDesc, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar_empty + 8 * s);
+            };
+            for (int i = 0; i < nstages; i += P) {
+                bool ready[2 * P];
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    const int t = i + p, s = t % kTcStages, par = (t / kTcStages) & 1;
+                    ready[2 * p] = mbar_try_wait(bar_tma + 8 * s, par);
+                    ready[2 * p + 1] = mbar_try_wait(bar_full + 8 * s, par);
+                }
+                bool ok = true;
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    const int t = i + p, s = t % kTcStages, par = (t / kTcStages) & 1;
+                    if (ok && !ready[2 * p]) ok = mbar_wait(bar_tma + 8 * s, par);
+                    if (ok && !ready[2 * p + 1]) ok = mbar_wait(bar_full + 8 * s, par);
+                }
+                if (!ok) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+                for (int p = 0; p < P; ++p) issue_stage(i + p);
             }
             // tracks every MMA issued above; also waited for here, so that no
             // MMA is in flight when the tensor memory is released, whether the
