@@ -8,36 +8,42 @@
 // the decoded weights go to the tensor cores instead of the FMA pipes:
 //
 //   D[n, m] (TMEM, fp32, 128 lanes x NB columns) += A[n, k] * B[m, k]^T
-//   A = decoded weight tile, 128 rows x 16 k, bf16, K-major, shared memory
+//   A = decoded weight tile, 128 rows x 16 k, bf16, K-major
 //   B = activation tile,      NB rows x 16 k, bf16, K-major, shared memory
 //
 // NB (the MMA's N) is 64, 128 or 256: one launch serves up to NB activation
 // rows, and larger M runs in NB-row chunks, each decoding the weights again.
-// One CTA owns 128 weight rows and the whole K range.  Its warps:
-//   * 16 decode warps write the bf16 weights of one 128-k stage into shared
-//     memory in the K-major 128-byte-swizzled layout: two k-blocks of 64 k,
-//     each row of a k-block 128 bytes, and inside every 8-row (1 KB) atom the
-//     16-byte chunk c of row r stored at chunk c ^ r.  The 8 lanes of one
-//     shared-memory phase write 8 different rows, so the XOR spreads their
-//     16-byte stores over all 32 banks.  The quotient is computed on the FMA
-//     pipe (two-part reciprocal, two windows per f32x2 instruction;
-//     trellis_device.cuh).
-//   * 1 TMA warp loads the activation tile of the stage with two 2-D tensor
-//     copies (one per k-block, 128-byte rows) that the TMA swizzles into the
-//     same layout.  The box covers the chunk's rows rounded up to 8; rows
-//     beyond it only feed accumulator columns that are never stored.
-//   * 1 MMA warp: one thread issues the 8 tcgen05.mma (K = 16 each) of a stage
-//     and commits them to the stage's "empty" barrier.
-// Two to four stages are in flight (mbarrier full/empty pairs).  After the
-// last stage the decode warps read the accumulator back with tcgen05.ld, round
-// to bf16 and store out[m, n] (each store instruction writes 32 consecutive n).
+// One CTA owns 128 weight rows and the whole K range, with 16 decode warps,
+// one TMA warp and one MMA warp (one thread issues the 8 tcgen05.mma, K = 16
+// each, of a 128-k stage and commits them to the stage's "empty" barrier).
+// Two kernels:
+//   * gemm_tca_kernel, the page's geometry (k in {2, 3, 4}, 12-bit windows):
+//     the TMA thread loads each block's code words for the CTA's 128 rows into
+//     shared memory next to the activation tiles; decode warp w takes weight
+//     rows 32*(w%4) .. +31 (one row a lane) and group w/4 of each stage, reads
+//     its words from shared memory and writes the decoded bf16 values straight
+//     into tensor memory (tcgen05.st), where the MMA takes A from.
+//   * gemm_tc_kernel, every other (k, L): decode warps load their code words
+//     from global memory and write the A tile to shared memory in the K-major
+//     128-byte-swizzled layout (two k-blocks of 64 k, each row of a k-block
+//     128 bytes, and inside every 8-row (1 KB) atom the 16-byte chunk c of row
+//     r stored at chunk c ^ r), published to the tensor cores by a proxy fence.
+// In both the quotient is computed on the FMA pipe (two-part reciprocal, two
+// windows per f32x2 instruction; trellis_device.cuh), the TMA warp loads each
+// stage's activation tile with two 2-D tensor copies (one per k-block,
+// 128-byte rows, swizzled by the TMA into the MMA's layout; the box covers the
+// chunk's rows rounded up to 8, and rows beyond it only feed accumulator
+// columns that are never stored), and after the last stage the decode warps
+// read the accumulator back with tcgen05.ld, round to bf16 and store out[m, n]
+// (each store instruction writes 32 consecutive n).
 //
 // Every mbarrier wait is bounded; a wait that runs out records an error in a
 // device word (read by trellis_device_status) and the CTA winds down without
-// leaving asynchronous work behind: the activation copies complete on
-// barriers of their own, which the TMA thread waits for (bounded) before it
-// leaves, and the MMA thread always commits and waits for its last MMAs, so
-// nothing is in flight when the tensor memory is released.
+// leaving asynchronous work behind: the TMA copies complete on barriers of
+// their own, which the TMA thread waits for (bounded) before it leaves, the
+// decode warps wait for their own tensor-memory stores, and the MMA thread
+// always commits and waits for its last MMAs, so nothing is in flight when the
+// tensor memory is released.
 #include <cuda.h>
 #include <cstdint>
 #include <mutex>
@@ -483,6 +489,305 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
     }
 }
 
+
+// ---- fast geometry: decoded tiles in tensor memory, code tiles by TMA -----
+// For k in {2, 3, 4} and 12-bit windows the decode warps take their code words
+// from shared memory, where the TMA thread puts each block's 128 rows x 32
+// words (128 bytes a row, 128-byte swizzled: the 16-byte chunk c of row r at
+// chunk c ^ (r % 8); for k < 4 the tile also holds the start of the next
+// block, unused), and write the decoded bf16 tile to tensor memory with
+// tcgen05.st: there the MMA reads A directly, so no shared-memory A tile and
+// no generic-to-async proxy fence are needed.  Tensor-memory lane = weight
+// row; a 32-bit column holds two consecutive k (the lower k in the low half).
+constexpr int kCodeTileWords = 32;
+constexpr int kCodeTileBytes = kTcRows * kCodeTileWords * 4;   // 16 KB
+constexpr int kCodeSlots = 3;
+
+template <int NB>
+struct TcaShape {
+    static constexpr int kStages = NB == 64 ? 6 : (NB == 128 ? 4 : 2);
+    static constexpr int kBBytes = NB * kTcStageK * 2;
+    static constexpr int kOffB = 0;
+    static constexpr int kOffCode = kOffB + kStages * kBBytes;
+    static constexpr int kOffBar = kOffCode + kCodeSlots * kCodeTileBytes;
+    static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarTma = 2 * kStages, kBarCode = 3 * kStages,
+                         kBarDone = 3 * kStages + kCodeSlots;
+    static constexpr int kOffTaddr = kOffBar + (kBarDone + 1) * 8;
+    static constexpr int kSmemBytes = kOffTaddr + 16 + 1024;
+    static constexpr int kAColBase = NB;          // accumulator: columns [0, NB)
+    static constexpr int kTmemCols = 512;
+    static_assert(NB + kStages * 64 <= kTmemCols, "tensor memory columns");
+    static_assert(kStages % 2 == 0 && kStages <= 2 * kCodeSlots, "stage pairs; code slot reuse");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
+    static_assert(kOffCode % 1024 == 0 && kBBytes % 1024 == 0 && kCodeTileBytes % 1024 == 0,
+                  "swizzle atoms must start on 1 KB boundaries");
+};
+
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+// Word w of this row in a code tile (row base `rb`, row index mod 8 `r7`).
+__device__ __forceinline__ uint32_t code_word_addr(uint32_t rb, uint32_t r7, int w) {
+    return rb + ((static_cast<uint32_t>(w >> 2) ^ r7) << 4) + (static_cast<uint32_t>(w & 3) << 2);
+}
+// The KB words of group g of the tile's block and its lookahead word (the
+// next word, or word 0 of the block for group 0).
+template <int KB>
+__device__ __forceinline__ void tile_group_words(uint32_t rb, uint32_t r7, int g, uint32_t (&w)[KB + 1]) {
+    const int w0 = (kGroupsPerBlock - 1 - g) * KB;
+    if constexpr (KB == 4) {
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(code_word_addr(rb, r7, w0)));
+    } else if constexpr (KB == 2) {
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(code_word_addr(rb, r7, w0)));
+    } else {
+#pragma unroll
+        for (int q = 0; q < KB; ++q) w[q] = lds32(code_word_addr(rb, r7, w0 + q));
+    }
+    w[KB] = lds32(code_word_addr(rb, r7, (w0 + KB) % (kGroupsPerBlock * KB)));
+}
+
+template <int KB, int NB>
+__global__ void __launch_bounds__(kTcThreads, 1)
+gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, int M, int K, int N,
+                const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap code_map) {
+    using S = TcaShape<NB>;
+    constexpr int kS = S::kStages;
+    constexpr int kBBytes = S::kBBytes;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sraw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    const uint32_t sbase = (sraw + 1023u) & ~1023u;
+    unsigned char* const smem = smem_raw + (sbase - sraw);
+    const uint32_t bar_full = sbase + S::kOffBar + 8 * S::kBarFull;
+    const uint32_t bar_empty = sbase + S::kOffBar + 8 * S::kBarEmpty;
+    const uint32_t bar_tma = sbase + S::kOffBar + 8 * S::kBarTma;
+    const uint32_t bar_code = sbase + S::kOffBar + 8 * S::kBarCode;
+    const uint32_t bar_done = sbase + S::kOffBar + 8 * S::kBarDone;
+    const int nstages = K / kTcStageK;
+    const int nblocks = nstages / 2;
+    const int n0 = blockIdx.x * kTcRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kS; ++s) {
+            mbar_init(bar_full + 8 * s, kTcDecodeWarps);
+            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_tma + 8 * s, 1);
+        }
+        for (int c = 0; c < kCodeSlots; ++c) mbar_init(bar_code + 8 * c, 1);
+        mbar_init(bar_done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_async_shared();
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(sbase + S::kOffTaddr), "r"(S::kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t taddr = *reinterpret_cast<volatile uint32_t*>(smem + S::kOffTaddr);
+    if (warp == kTcTmaWarp && lane == 0) {
+        // L2 prefetches of the first code tiles (no data reaches the CTA
+        // before the wait for the previous grid; L2 cannot hold a stale line)
+        for (int b = 0; b < kCodeSlots && b < nblocks; ++b)
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                         :: "l"(reinterpret_cast<uint64_t>(&code_map)), "r"(b * kGroupsPerBlock * KB), "r"(n0)
+                         : "memory");
+    }
+    griddep_wait();
+
+    if (warp < kTcDecodeWarps) {
+        // ---------------------------------------------------------------- decode
+        // warp w: tensor-memory lanes (weight rows) 32*(w%4) .. +31, group
+        // gi = w/4 of each stage's four 32-k groups (A columns 16*gi .. +15)
+        const int q4 = warp & 3, gi = warp >> 2;
+        const int row_local = 32 * q4 + lane;
+        const int row = n0 + row_local;
+        const float sr = row < N ? bf16_bits_to_f32(__ldg(scales + row)) : 0.0f;
+        const float2 s2 = make_float2(sr, sr);
+        const uint32_t r7 = static_cast<uint32_t>(row_local & 7);
+        const uint32_t rb0 = sbase + S::kOffCode + static_cast<uint32_t>(row_local * kCodeTileWords * 4);
+        const uint32_t t_row = taddr + (static_cast<uint32_t>(32 * q4) << 16) +
+                               static_cast<uint32_t>(S::kAColBase + 16 * gi);
+        bool alive = true;
+        int c = 0, cpar = 0;     // code slot of block b and its phase parity
+        int se = 0;              // A slot of the even stage 2b
+        int spar = 1;            // parity the odd stage's slot probe waits for
+        for (int b = 0; b < nblocks; ++b) {
+            // The block's code tile, and the A slot of the odd stage 2b + 1:
+            // the commit that frees it (MMAs of stage 2b + 1 - kS) tracks every
+            // earlier MMA, those of stage 2b - kS (the even slot's previous
+            // user) included.  Odd slots are probed at every one of their
+            // phases, even slots never.  Both probes are issued before either
+            // result is used, so their latencies overlap.
+            const bool probe_slot = 2 * b + 1 >= kS;
+            const bool code_ready = mbar_try_wait(bar_code + 8 * c, static_cast<uint32_t>(cpar));
+            const bool slot_ready = !probe_slot || mbar_try_wait(bar_empty + 8 * (se + 1), static_cast<uint32_t>(spar));
+            if (!code_ready) alive = mbar_wait(bar_code + 8 * c, static_cast<uint32_t>(cpar));
+            if (alive && !slot_ready) alive = mbar_wait(bar_empty + 8 * (se + 1), static_cast<uint32_t>(spar));
+            if (!alive) break;
+            const uint32_t rb = rb0 + static_cast<uint32_t>(c * kCodeTileBytes);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t w[KB + 1];
+                tile_group_words<KB>(rb, r7, 4 * h + gi, w);
+                uint32_t packed[16];
+#pragma unroll
+                for (int jp = 0; jp < 16; ++jp) {
+                    const float2 v = window_value2(group_window<KB, kL>(w, 2 * jp), group_window<KB, kL>(w, 2 * jp + 1));
+                    const float2 ws = __fmul2_rn(v, s2);
+                    packed[jp] = pack_bf16x2(ws.x, ws.y);
+                }
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+                    "%11, %12, %13, %14, %15, %16};"
+                    :: "r"(t_row + static_cast<uint32_t>(64 * (se + h))), "r"(packed[0]), "r"(packed[1]),
+                       "r"(packed[2]), "r"(packed[3]), "r"(packed[4]), "r"(packed[5]), "r"(packed[6]),
+                       "r"(packed[7]), "r"(packed[8]), "r"(packed[9]), "r"(packed[10]), "r"(packed[11]),
+                       "r"(packed[12]), "r"(packed[13]), "r"(packed[14]), "r"(packed[15])
+                    : "memory");
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar_full + 8 * se);
+                mbar_arrive(bar_full + 8 * (se + 1));
+            }
+            if (++c == kCodeSlots) { c = 0; cpar ^= 1; }
+            se += 2;
+            if (se == kS) se = 0;
+            if (2 * b + 3 >= kS && ((2 * b + 3) % kS) == 1) spar ^= 1;
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+
+        // -------------------------------------------------------------- epilogue
+        const bool done = alive && mbar_wait(bar_done, 0);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const int sub = warp & 3, colq = warp >> 2;
+#pragma unroll
+        for (int cc = 0; cc < NB / 64 && done; ++cc) {
+            const int col = colq * (NB / 4) + 16 * cc;
+            uint32_t r[16];
+            const uint32_t ta = taddr + (static_cast<uint32_t>(32 * sub) << 16) + static_cast<uint32_t>(col);
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                "%12, %13, %14, %15}, [%16];"
+                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                  "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                  "=r"(r[14]), "=r"(r[15])
+                : "r"(ta));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            const int n = n0 + 32 * sub + lane;
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (col + j < M)
+                        out[static_cast<size_t>(col + j) * N + n] = bf16_bits_rn(__uint_as_float(r[j]));
+            }
+        }
+    } else if (warp == kTcTmaWarp) {
+        // ------------------------------------------------- x and code tiles via TMA
+        if (lane == 0) {
+            const int rows = tc_box_rows(M, NB);
+            int code_next = 0;
+            auto issue_code = [&](int b) {
+                const int cs = b % kCodeSlots;
+                mbar_arrive_expect_tx(bar_code + 8 * cs, static_cast<uint32_t>(kCodeTileBytes));
+                tma_load_2d(sbase + S::kOffCode + cs * kCodeTileBytes, &code_map, b * kGroupsPerBlock * KB, n0,
+                            bar_code + 8 * cs);
+            };
+            for (; code_next < kCodeSlots && code_next < nblocks; ++code_next) issue_code(code_next);
+            int issued = 0;
+            for (int i = 0; i < nstages; ++i) {
+                const int s = i % kS;
+                if (i >= kS && !mbar_wait(bar_empty + 8 * s, ((i / kS) + 1) & 1)) break;
+                mbar_arrive_expect_tx(bar_tma + 8 * s, static_cast<uint32_t>(2 * rows * kSwRowBytes));
+                const uint32_t dst = sbase + S::kOffB + s * kBBytes;
+#pragma unroll
+                for (int kb = 0; kb < kTcStageK / kSwK; ++kb)
+                    tma_load_2d(dst + kb * (NB * kSwRowBytes), &x_map, i * kTcStageK + kb * kSwK, 0,
+                                bar_tma + 8 * s);
+                issued = i + 1;
+                // The MMAs of stage i - kS are complete (waited above), so the
+                // decode of every stage up to i - kS is too: block p's code
+                // slot (that of block p - kCodeSlots) is free once stage
+                // 2 (p - kCodeSlots) + 1 <= i - kS.
+                if (i >= kS) {
+                    const int lim = ((i - kS - 1) >> 1) + kCodeSlots;
+                    for (; code_next <= lim && code_next < nblocks; ++code_next) issue_code(code_next);
+                }
+            }
+            // every copy issued has landed before the CTA can exit
+            for (int i = issued > kS ? issued - kS : 0; i < issued; ++i)
+                (void)mbar_wait(bar_tma + 8 * (i % kS), (i / kS) & 1);
+            for (int b = code_next > kCodeSlots ? code_next - kCodeSlots : 0; b < code_next; ++b)
+                (void)mbar_wait(bar_code + 8 * (b % kCodeSlots), (b / kCodeSlots) & 1);
+        }
+    } else {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint64_t db0 = smem_desc(sbase + S::kOffB);
+            const uint32_t db_hi = static_cast<uint32_t>(db0 >> 32);
+            auto issue_stage = [&](int i) {
+                const int s = i % kS;
+                const uint32_t ta_s = taddr + static_cast<uint32_t>(S::kAColBase + 64 * s);
+                const uint32_t db_s = static_cast<uint32_t>(db0) + static_cast<uint32_t>(s * (kBBytes >> 4));
+#pragma unroll
+                for (int kk = 0; kk < kTcStageK / 16; ++kk) {
+                    const int kb = kk / (kSwK / 16), ks = kk % (kSwK / 16);
+                    const uint32_t b_lo = db_s + static_cast<uint32_t>((kb * (NB * kSwRowBytes) + ks * 32) >> 4);
+                    mma_bf16_ta(taddr, ta_s + static_cast<uint32_t>(8 * kk),
+                                (static_cast<uint64_t>(db_hi) << 32) | b_lo, TcShape<NB>::kInstrDesc,
+                                (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar_empty + 8 * s);
+            };
+            for (int i = 0; i < nstages; i += 2) {
+                bool ready[4];
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int t = i + p, s = t % kS, par = (t / kS) & 1;
+                    ready[2 * p] = mbar_try_wait(bar_tma + 8 * s, par);
+                    ready[2 * p + 1] = mbar_try_wait(bar_full + 8 * s, par);
+                }
+                bool ok = true;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int t = i + p, s = t % kS, par = (t / kS) & 1;
+                    if (ok && !ready[2 * p]) ok = mbar_wait(bar_tma + 8 * s, par);
+                    if (ok && !ready[2 * p + 1]) ok = mbar_wait(bar_full + 8 * s, par);
+                }
+                if (!ok) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                issue_stage(i);
+                issue_stage(i + 1);
+            }
+            mma_commit(bar_done);
+            (void)mbar_wait(bar_done, 0);
+        }
+    }
+
+    griddep_launch_dependents();
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(S::kTmemCols)
+                     : "memory");
+    }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -537,6 +842,52 @@ int launch_tc_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* s
     return 0;
 }
 
+
+// codes [N, row_words] uint32 as a 2-D tensor (word, row) with a box of 32
+// words (128 bytes) x 128 rows, 128-byte swizzled; rows past N and words past
+// the row's end are filled with zeros.
+bool make_code_map(CUtensorMap* map, const uint32_t* codes, int N, int row_words) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_words), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_words) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kCodeTileWords), static_cast<cuuint32_t>(kTcRows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(codes), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KB, int NB>
+int launch_tca_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
+                      uint16_t* out, cudaStream_t stream) {
+    static std::atomic<unsigned long long> opted{0};
+    if (!smem_opt_in(gemm_tca_kernel<KB, NB>, TcaShape<NB>::kSmemBytes, opted)) return -5;
+    const int grid = (N + kTcRows - 1) / kTcRows;
+    CUtensorMap cmap;
+    if (!make_code_map(&cmap, codes, N, K / 32 * KB)) return -5;
+    for (int m = 0; m < M; m += NB) {
+        const int m0 = (M > NB && m + NB > M) ? M - NB : m;
+        const int mc = (M - m0) < NB ? (M - m0) : NB;
+        CUtensorMap map;
+        if (!make_x_map(&map, x + static_cast<size_t>(m0) * K, mc, K, tc_box_rows(mc, NB))) return -5;
+        const cudaError_t e = launch_programmatic(gemm_tca_kernel<KB, NB>, static_cast<unsigned>(grid),
+                                                  static_cast<unsigned>(kTcThreads), TcaShape<NB>::kSmemBytes,
+                                                  stream, scales, out + static_cast<size_t>(m0) * N, mc, K, N, map,
+                                                  cmap);
+        if (e != cudaSuccess) return -5;
+    }
+    return 0;
+}
+
+template <int KB>
+int launch_tca_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
+                        uint16_t* out, cudaStream_t stream) {
+    if (M <= 64) return launch_tca_chunks<KB, 64>(x, codes, scales, M, K, N, out, stream);
+    if (M <= 128) return launch_tca_chunks<KB, 128>(x, codes, scales, M, K, N, out, stream);
+    return launch_tca_chunks<KB, 256>(x, codes, scales, M, K, N, out, stream);
+}
+
 // The MMA's N follows M: 64 for M <= 64, 128 for M <= 128, else 256.  Above
 // 256 rows the launches take 256-row chunks (each decodes the weights again;
 // they are programmatically chained on the stream), and the last chunk is
@@ -558,9 +909,9 @@ int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* sca
                    int L, uint16_t* out, cudaStream_t stream) {
     if (fast_geometry(k, L)) {
         switch (k) {
-            case 2: return launch_tc_instance<2, kL>(x, codes, scales, M, K, N, L, out, stream);
-            case 3: return launch_tc_instance<3, kL>(x, codes, scales, M, K, N, L, out, stream);
-            default: return launch_tc_instance<4, kL>(x, codes, scales, M, K, N, L, out, stream);
+            case 2: return launch_tca_instance<2>(x, codes, scales, M, K, N, out, stream);
+            case 3: return launch_tca_instance<3>(x, codes, scales, M, K, N, out, stream);
+            default: return launch_tca_instance<4>(x, codes, scales, M, K, N, out, stream);
         }
     }
     switch (k) {
