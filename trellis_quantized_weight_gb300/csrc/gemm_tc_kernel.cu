@@ -28,14 +28,17 @@
 //     128-byte-swizzled layout (two k-blocks of 64 k, each row of a k-block
 //     128 bytes, and inside every 8-row (1 KB) atom the 16-byte chunk c of row
 //     r stored at chunk c ^ r), published to the tensor cores by a proxy fence.
-// In both the quotient is computed on the FMA pipe (two-part reciprocal, two
-// windows per f32x2 instruction; trellis_device.cuh), the TMA warp loads each
-// stage's activation tile with two 2-D tensor copies (one per k-block,
-// 128-byte rows, swizzled by the TMA into the MMA's layout; the box covers the
-// chunk's rows rounded up to 8, and rows beyond it only feed accumulator
-// columns that are never stored), and after the last stage the decode warps
-// read the accumulator back with tcgen05.ld, round to bf16 and store out[m, n]
-// (each store instruction writes 32 consecutive n).
+// The quotient: with NB = 64 the tensor-memory kernel reads it from the
+// per-lane shared-memory table of the CUDA-core kernel (one dp4a address and
+// one load a window, indexed by the hash's byte sum; trellis_device.cuh), which
+// its freed shared memory now holds; otherwise it is computed on the FMA pipe
+// (two-part reciprocal, two windows per f32x2 instruction).  In both kernels
+// the TMA warp loads each stage's activation tile with two 2-D tensor copies
+// (one per k-block, 128-byte rows, swizzled by the TMA into the MMA's layout;
+// the box covers the chunk's rows rounded up to 8, and rows beyond it only feed
+// accumulator columns that are never stored), and after the last stage the
+// decode warps read the accumulator back with tcgen05.ld, round to bf16 and
+// store out[m, n] (each store instruction writes 32 consecutive n).
 //
 // Every mbarrier wait is bounded; a wait that runs out records an error in a
 // device word (read by trellis_device_status) and the CTA winds down without
@@ -64,11 +67,9 @@ constexpr int kTcThreads = (kTcDecodeWarps + 2) * 32;
 constexpr int kTcTmaWarp = kTcDecodeWarps;
 constexpr int kTcMmaWarp = kTcDecodeWarps + 1;
 
-// The quotient is computed (window_value2), not read from the per-lane
-// shared-memory table of the CUDA-core kernel: this kernel's
-// shared-memory pipe carries the A tiles, the activation tiles and the tensor
-// cores' operand reads, while its issue slots have room, and the table's
-// 113 KB of shared memory goes to deeper pipelining instead.
+// The shared-memory-A kernel computes the quotient (window_value2) rather
+// than reading the per-lane table of the CUDA-core kernel: its A tiles take
+// the shared memory the table's 113 KB would need.
 
 constexpr int kABytes = kTcRows * kTcStageK * 2;     // 32 KB
 constexpr int kSwK = 64;                             // k per 128-byte swizzled row (one k-block)
@@ -503,13 +504,16 @@ constexpr int kCodeTileWords = 32;
 constexpr int kCodeTileBytes = kTcRows * kCodeTileWords * 4;   // 16 KB
 constexpr int kCodeSlots = 3;
 
-template <int NB>
+// TAB: the quotient comes from the per-lane shared-memory table (NB = 64,
+// where the table, three code slots and four activation slots fit in 227 KB).
+template <int NB, bool TAB>
 struct TcaShape {
-    static constexpr int kStages = NB == 64 ? 6 : (NB == 128 ? 4 : 2);
+    static constexpr int kStages = TAB ? 4 : (NB == 64 ? 6 : (NB == 128 ? 4 : 2));
     static constexpr int kBBytes = NB * kTcStageK * 2;
     static constexpr int kOffB = 0;
     static constexpr int kOffCode = kOffB + kStages * kBBytes;
-    static constexpr int kOffBar = kOffCode + kCodeSlots * kCodeTileBytes;
+    static constexpr int kOffTable = kOffCode + kCodeSlots * kCodeTileBytes;
+    static constexpr int kOffBar = kOffTable + (TAB ? kQuotientTableBytes : 0);
     static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarTma = 2 * kStages, kBarCode = 3 * kStages,
                          kBarDone = 3 * kStages + kCodeSlots;
     static constexpr int kOffTaddr = kOffBar + (kBarDone + 1) * 8;
@@ -555,11 +559,11 @@ __device__ __forceinline__ void tile_group_words(uint32_t rb, uint32_t r7, int g
     w[KB] = lds32(code_word_addr(rb, r7, (w0 + KB) % (kGroupsPerBlock * KB)));
 }
 
-template <int KB, int NB>
+template <int KB, int NB, bool TAB>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, int M, int K, int N,
                 const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap code_map) {
-    using S = TcaShape<NB>;
+    using S = TcaShape<NB, TAB>;
     constexpr int kS = S::kStages;
     constexpr int kBBytes = S::kBBytes;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -587,6 +591,7 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_async_shared();
     }
+    if constexpr (TAB) build_quotient_table(reinterpret_cast<float*>(smem + S::kOffTable), threadIdx.x, kTcThreads);
     if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      :: "r"(sbase + S::kOffTaddr), "r"(S::kTmemCols) : "memory");
@@ -619,6 +624,7 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
         const uint32_t rb0 = sbase + S::kOffCode + static_cast<uint32_t>(row_local * kCodeTileWords * 4);
         const uint32_t t_row = taddr + (static_cast<uint32_t>(32 * q4) << 16) +
                                static_cast<uint32_t>(S::kAColBase + 16 * gi);
+        const uint32_t lane_tbl = quotient_table_lane_address(smem + S::kOffTable, lane);
         bool alive = true;
         int c = 0, cpar = 0;     // code slot of block b and its phase parity
         int se = 0;              // A slot of the even stage 2b
@@ -644,7 +650,13 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
                 uint32_t packed[16];
 #pragma unroll
                 for (int jp = 0; jp < 16; ++jp) {
-                    const float2 v = window_value2(group_window<KB, kL>(w, 2 * jp), group_window<KB, kL>(w, 2 * jp + 1));
+                    float2 v;
+                    if constexpr (TAB) {
+                        v.x = quotient_lookup(group_window<KB, kL>(w, 2 * jp), lane_tbl);
+                        v.y = quotient_lookup(group_window<KB, kL>(w, 2 * jp + 1), lane_tbl);
+                    } else {
+                        v = window_value2(group_window<KB, kL>(w, 2 * jp), group_window<KB, kL>(w, 2 * jp + 1));
+                    }
                     const float2 ws = __fmul2_rn(v, s2);
                     packed[jp] = pack_bf16x2(ws.x, ws.y);
                 }
@@ -858,11 +870,11 @@ bool make_code_map(CUtensorMap* map, const uint32_t* codes, int N, int row_words
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KB, int NB>
+template <int KB, int NB, bool TAB>
 int launch_tca_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
                       uint16_t* out, cudaStream_t stream) {
     static std::atomic<unsigned long long> opted{0};
-    if (!smem_opt_in(gemm_tca_kernel<KB, NB>, TcaShape<NB>::kSmemBytes, opted)) return -5;
+    if (!smem_opt_in(gemm_tca_kernel<KB, NB, TAB>, TcaShape<NB, TAB>::kSmemBytes, opted)) return -5;
     const int grid = (N + kTcRows - 1) / kTcRows;
     CUtensorMap cmap;
     if (!make_code_map(&cmap, codes, N, K / 32 * KB)) return -5;
@@ -871,8 +883,8 @@ int launch_tca_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* 
         const int mc = (M - m0) < NB ? (M - m0) : NB;
         CUtensorMap map;
         if (!make_x_map(&map, x + static_cast<size_t>(m0) * K, mc, K, tc_box_rows(mc, NB))) return -5;
-        const cudaError_t e = launch_programmatic(gemm_tca_kernel<KB, NB>, static_cast<unsigned>(grid),
-                                                  static_cast<unsigned>(kTcThreads), TcaShape<NB>::kSmemBytes,
+        const cudaError_t e = launch_programmatic(gemm_tca_kernel<KB, NB, TAB>, static_cast<unsigned>(grid),
+                                                  static_cast<unsigned>(kTcThreads), TcaShape<NB, TAB>::kSmemBytes,
                                                   stream, scales, out + static_cast<size_t>(m0) * N, mc, K, N, map,
                                                   cmap);
         if (e != cudaSuccess) return -5;
@@ -883,9 +895,9 @@ int launch_tca_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* 
 template <int KB>
 int launch_tca_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
                         uint16_t* out, cudaStream_t stream) {
-    if (M <= 64) return launch_tca_chunks<KB, 64>(x, codes, scales, M, K, N, out, stream);
-    if (M <= 128) return launch_tca_chunks<KB, 128>(x, codes, scales, M, K, N, out, stream);
-    return launch_tca_chunks<KB, 256>(x, codes, scales, M, K, N, out, stream);
+    if (M <= 64) return launch_tca_chunks<KB, 64, true>(x, codes, scales, M, K, N, out, stream);
+    if (M <= 128) return launch_tca_chunks<KB, 128, false>(x, codes, scales, M, K, N, out, stream);
+    return launch_tca_chunks<KB, 256, false>(x, codes, scales, M, K, N, out, stream);
 }
 
 // The MMA's N follows M: 64 for M <= 64, 128 for M <= 128, else 256.  Above
