@@ -668,12 +668,20 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
                        "r"(packed[7]), "r"(packed[8]), "r"(packed[9]), "r"(packed[10]), "r"(packed[11]),
                        "r"(packed[12]), "r"(packed[13]), "r"(packed[14]), "r"(packed[15])
                     : "memory");
+                if (h == 0 && b + 1 == nblocks) {
+                    // the last block's even stage is published on its own, so
+                    // that its MMAs overlap the odd stage's decode
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_full + 8 * se);
+                }
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(bar_full + 8 * se);
+                if (b + 1 < nblocks) mbar_arrive(bar_full + 8 * se);
                 mbar_arrive(bar_full + 8 * (se + 1));
             }
             if (++c == kCodeSlots) { c = 0; cpar ^= 1; }
@@ -765,6 +773,10 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
                 }
                 mma_commit(bar_empty + 8 * s);
             };
+            // Stages are published in pairs (the last pair stage by stage), so
+            // the four barrier probes of a pair are issued back to back (their
+            // latencies overlap), and each stage's MMAs go out as soon as its
+            // own barriers have completed.
             for (int i = 0; i < nstages; i += 2) {
                 bool ready[4];
 #pragma unroll
@@ -779,11 +791,11 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
                     const int t = i + p, s = t % kS, par = (t / kS) & 1;
                     if (ok && !ready[2 * p]) ok = mbar_wait(bar_tma + 8 * s, par);
                     if (ok && !ready[2 * p + 1]) ok = mbar_wait(bar_full + 8 * s, par);
+                    if (!ok) break;
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    issue_stage(t);
                 }
                 if (!ok) break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                issue_stage(i);
-                issue_stage(i + 1);
             }
             mma_commit(bar_done);
             (void)mbar_wait(bar_done, 0);
