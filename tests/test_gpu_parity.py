@@ -105,7 +105,7 @@ def test_gemm_m64_tensor_cores(tq, oracle_lib, k, N, K):
 
 
 @pytest.mark.parametrize("M", [17, 33, 63, 65, 100, 128, 129, 200, 256, 257, 300, 513])
-@pytest.mark.parametrize("k", [2, 4])
+@pytest.mark.parametrize("k", [2, 3, 4])
 def test_gemm_general_m_tensor_cores(tq, oracle_lib, M, k):
     """M > 16 runs on tcgen05 with the MMA's N = 64, 128 or 256 (chunks of 256
     rows above that, the last one overlapping); a partial chunk's missing rows
@@ -201,10 +201,12 @@ def test_gemm_gateup_without_activation(tq, oracle_lib):
         assert_gemm_close(host_bits(got), ref, refabs, what)
 
 
-def test_gemm_m64_one_hot_is_exact(tq, oracle_lib):
-    """Each of the 64 rows of x selects a different weight column, bit for bit."""
-    N, K, k = 256, 1024, 4
-    _, codes, scales = _inputs(1, K, N, k, seed=641)
+@pytest.mark.parametrize("k", [2, 3, 4])
+def test_gemm_m64_one_hot_is_exact(tq, oracle_lib, k):
+    """Each of the 64 rows of x selects a different weight column, bit for bit
+    (every k, so every code-word layout of the tensor-core decode)."""
+    N, K = 256, 1024
+    _, codes, scales = _inputs(1, K, N, k, seed=641 + k)
     w = oracle_lib.decode(codes, scales, K, N, k)
     cols = [(37 * i + 5) % K for i in range(64)]
     e = np.zeros((64, K), np.uint16)
