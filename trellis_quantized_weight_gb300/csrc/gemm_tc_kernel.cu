@@ -17,13 +17,15 @@
 // one TMA warp and one MMA warp (one thread issues the 8 tcgen05.mma, K = 16
 // each, of a 128-k stage and commits them to the stage's "empty" barrier).
 // Two kernels:
-//   * gemm_tca_kernel, the page's geometry (k in {2, 3, 4}, 12-bit windows):
-//     the TMA thread loads each block's code words for the CTA's 128 rows into
+//   * gemm_tca_kernel, the page's geometry (k in {2, 3, 4}, 12-bit windows)
+//     with NB = 64 or 128: the TMA thread loads each block's code words for the
+//     CTA's 128 rows into
 //     shared memory next to the activation tiles; decode warp w takes weight
 //     rows 32*(w%4) .. +31 (one row a lane) and group w/4 of each stage, reads
 //     its words from shared memory and writes the decoded bf16 values straight
 //     into tensor memory (tcgen05.st), where the MMA takes A from.
-//   * gemm_tc_kernel, every other (k, L): decode warps load their code words
+//   * gemm_tc_kernel, every other (k, L), and NB = 256 (where 64 KB activation
+//     tiles leave room for two stages only): decode warps load their code words
 //     from global memory and write the A tile to shared memory in the K-major
 //     128-byte-swizzled layout (two k-blocks of 64 k, each row of a k-block
 //     128 bytes, and inside every 8-row (1 KB) atom the 16-byte chunk c of row
@@ -508,7 +510,7 @@ constexpr int kCodeSlots = 3;
 // where the table, three code slots and four activation slots fit in 227 KB).
 template <int NB, bool TAB>
 struct TcaShape {
-    static constexpr int kStages = TAB ? 4 : (NB == 64 ? 6 : (NB == 128 ? 4 : 2));
+    static constexpr int kStages = TAB ? 4 : (NB == 64 ? 6 : 4);
     static constexpr int kBBytes = NB * kTcStageK * 2;
     static constexpr int kOffB = 0;
     static constexpr int kOffCode = kOffB + kStages * kBBytes;
@@ -520,6 +522,7 @@ struct TcaShape {
     static constexpr int kSmemBytes = kOffTaddr + 16 + 1024;
     static constexpr int kAColBase = NB;          // accumulator: columns [0, NB)
     static constexpr int kTmemCols = 512;
+    static_assert(NB == 64 || NB == 128, "MMA N of this kernel");
     static_assert(NB + kStages * 64 <= kTmemCols, "tensor memory columns");
     static_assert(kStages % 2 == 0 && kStages <= 2 * kCodeSlots, "stage pairs; code slot reuse");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
@@ -909,7 +912,12 @@ int launch_tca_instance(const uint16_t* x, const uint32_t* codes, const uint16_t
                         uint16_t* out, cudaStream_t stream) {
     if (M <= 64) return launch_tca_chunks<KB, 64, true>(x, codes, scales, M, K, N, out, stream);
     if (M <= 128) return launch_tca_chunks<KB, 128, false>(x, codes, scales, M, K, N, out, stream);
-    return launch_tca_chunks<KB, 256, false>(x, codes, scales, M, K, N, out, stream);
+    // 256 activation rows: 64 KB activation tiles leave shared memory for two
+    // stages only, and with two tensor-memory A slots the decode of a pair
+    // cannot start before the previous pair's MMAs are done (M = 256:
+    // 56.3 us against 43.4 for the shared-memory-A kernel, which overlaps them
+    // within its two stages), so these chunks take the shared-memory-A kernel
+    return launch_tc_chunks<KB, 256, kL>(x, codes, scales, M, K, N, (1u << kL) - 1u, out, stream);
 }
 
 // The MMA's N follows M: 64 for M <= 64, 128 for M <= 128, else 256.  Above
