@@ -47,7 +47,7 @@ def test_decode_general_geometry_bitexact(tq, oracle_lib, k, L):
 
 
 @pytest.mark.parametrize("k,L", [(1, 2), (1, 12), (2, 16), (3, 7), (4, 24), (5, 12), (6, 9), (7, 20), (8, 24)])
-@pytest.mark.parametrize("M", [1, 3, 8, 13, 16, 17, 64, 200])
+@pytest.mark.parametrize("M", [1, 3, 8, 13, 16, 17, 64, 100, 200])
 def test_gemm_general_geometry(tq, oracle_lib, k, L, M):
     import torch
     from trellis_quantized_weight_gb300 import binding
@@ -81,7 +81,7 @@ def test_gemm_general_two_row_shapes(tq, oracle_lib, k, L, M):
     assert_gemm_close(got, ref, refabs, f"M={M} k={k} L={L}")
 
 
-@pytest.mark.parametrize("k,L,M", [(1, 24, 16), (5, 16, 9), (8, 10, 40), (7, 12, 256)])
+@pytest.mark.parametrize("k,L,M", [(1, 24, 16), (5, 16, 9), (8, 10, 40), (6, 16, 100), (7, 12, 256)])
 def test_gemm_general_one_hot_rows_are_exact(tq, oracle_lib, k, L, M):
     """Row i of x selects weight column j_i: each output row is that decoded
     column bit for bit (one exact product plus zeros)."""

@@ -17,20 +17,21 @@
 // one TMA warp and one MMA warp (one thread issues the 8 tcgen05.mma, K = 16
 // each, of a 128-k stage and commits them to the stage's "empty" barrier).
 // Two kernels:
-//   * gemm_tca_kernel, the page's geometry (k in {2, 3, 4}, 12-bit windows)
-//     with NB = 64 or 128: the TMA thread loads each block's code words for the
-//     CTA's 128 rows into
-//     shared memory next to the activation tiles; decode warp w takes weight
-//     rows 32*(w%4) .. +31 (one row a lane) and group w/4 of each stage, reads
-//     its words from shared memory and writes the decoded bf16 values straight
-//     into tensor memory (tcgen05.st), where the MMA takes A from.
-//   * gemm_tc_kernel, every other (k, L), and NB = 256 (where 64 KB activation
-//     tiles leave room for two stages only): decode warps load their code words
-//     from global memory and write the A tile to shared memory in the K-major
+//   * gemm_tca_kernel, k = 2 .. 8 with NB = 64 or 128: the TMA thread loads
+//     each block's code words (one or two 128-byte boxes a row) for the CTA's
+//     128 rows into shared memory next to the activation tiles; decode warp w
+//     takes weight rows 32*(w%4) .. +31 (one row a lane) and group w/4 of each
+//     stage, reads its words from shared memory and writes the decoded bf16
+//     values straight into tensor memory (tcgen05.st), where the MMA takes A
+//     from.
+//   * gemm_tc_kernel, NB = 256 (where 64 KB activation tiles leave room for
+//     two stages only) and k = 1: decode warps load their code words from
+//     global memory and write the A tile to shared memory in the K-major
 //     128-byte-swizzled layout (two k-blocks of 64 k, each row of a k-block
 //     128 bytes, and inside every 8-row (1 KB) atom the 16-byte chunk c of row
 //     r stored at chunk c ^ r), published to the tensor cores by a proxy fence.
-// The quotient: with NB = 64 the tensor-memory kernel reads it from the
+// The quotient: with NB = 64 and the page's geometry (k in {2, 3, 4}, 12-bit
+// windows) the tensor-memory kernel reads it from the
 // per-lane shared-memory table of the CUDA-core kernel (one dp4a address and
 // one load a window, indexed by the hash's byte sum; trellis_device.cuh), which
 // its freed shared memory now holds; otherwise it is computed on the FMA pipe
@@ -493,28 +494,34 @@ gemm_tc_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ 
 }
 
 
-// ---- fast geometry: decoded tiles in tensor memory, code tiles by TMA -----
-// For k in {2, 3, 4} and 12-bit windows the decode warps take their code words
-// from shared memory, where the TMA thread puts each block's 128 rows x 32
-// words (128 bytes a row, 128-byte swizzled: the 16-byte chunk c of row r at
-// chunk c ^ (r % 8); for k < 4 the tile also holds the start of the next
-// block, unused), and write the decoded bf16 tile to tensor memory with
-// tcgen05.st: there the MMA reads A directly, so no shared-memory A tile and
-// no generic-to-async proxy fence are needed.  Tensor-memory lane = weight
-// row; a 32-bit column holds two consecutive k (the lower k in the low half).
-constexpr int kCodeTileWords = 32;
+// ---- decoded tiles in tensor memory, code tiles by TMA ---------------------
+// The decode warps take their code words from shared memory, where the TMA
+// thread puts each block's 128 rows x 8k words as one or two boxes of 32 words
+// (128 bytes a row, 128-byte swizzled: the 16-byte chunk c of row r at chunk
+// c ^ (r % 8); a box past the block's words holds the start of the next block,
+// unused, or zeros past the row's end), and write the decoded bf16 tile to
+// tensor memory with tcgen05.st: there the MMA reads A directly, so no
+// shared-memory A tile and no generic-to-async proxy fence are needed.
+// Tensor-memory lane = weight row; a 32-bit column holds two consecutive k (the
+// lower k in the low half).
+constexpr int kCodeTileWords = 32;                             // one TMA box: 128 bytes a row
 constexpr int kCodeTileBytes = kTcRows * kCodeTileWords * 4;   // 16 KB
 constexpr int kCodeSlots = 3;
+// boxes a block's code words take: its 8k words (one box for k <= 4, two above)
+__host__ __device__ constexpr int code_boxes(int kb) {
+    return (kGroupsPerBlock * kb + kCodeTileWords - 1) / kCodeTileWords;
+}
 
 // TAB: the quotient comes from the per-lane shared-memory table (NB = 64,
 // where the table, three code slots and four activation slots fit in 227 KB).
-template <int NB, bool TAB>
+template <int NB, bool TAB, int KB>
 struct TcaShape {
     static constexpr int kStages = TAB ? 4 : (NB == 64 ? 6 : 4);
     static constexpr int kBBytes = NB * kTcStageK * 2;
+    static constexpr int kCodeBytes = code_boxes(KB) * kCodeTileBytes;   // one code slot
     static constexpr int kOffB = 0;
     static constexpr int kOffCode = kOffB + kStages * kBBytes;
-    static constexpr int kOffTable = kOffCode + kCodeSlots * kCodeTileBytes;
+    static constexpr int kOffTable = kOffCode + kCodeSlots * kCodeBytes;
     static constexpr int kOffBar = kOffTable + (TAB ? kQuotientTableBytes : 0);
     static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarTma = 2 * kStages, kBarCode = 3 * kStages,
                          kBarDone = 3 * kStages + kCodeSlots;
@@ -526,7 +533,8 @@ struct TcaShape {
     static_assert(NB + kStages * 64 <= kTmemCols, "tensor memory columns");
     static_assert(kStages % 2 == 0 && kStages <= 2 * kCodeSlots, "stage pairs; code slot reuse");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
-    static_assert(kOffCode % 1024 == 0 && kBBytes % 1024 == 0 && kCodeTileBytes % 1024 == 0,
+    static_assert(!TAB || KB <= 4, "the quotient table serves 12-bit windows of k <= 4");
+    static_assert(kOffCode % 1024 == 0 && kBBytes % 1024 == 0 && kCodeBytes % 1024 == 0,
                   "swizzle atoms must start on 1 KB boundaries");
 };
 
@@ -541,18 +549,24 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
 }
-// Word w of this row in a code tile (row base `rb`, row index mod 8 `r7`).
+// Word w of this row in a code slot (row base `rb` in the slot's first box,
+// row index mod 8 `r7`): box w / 32, 16-byte chunk (w % 32) / 4 swizzled.
 __device__ __forceinline__ uint32_t code_word_addr(uint32_t rb, uint32_t r7, int w) {
-    return rb + ((static_cast<uint32_t>(w >> 2) ^ r7) << 4) + (static_cast<uint32_t>(w & 3) << 2);
+    return rb + (static_cast<uint32_t>(w >> 5) * kCodeTileBytes) + ((static_cast<uint32_t>((w >> 2) & 7) ^ r7) << 4) +
+           (static_cast<uint32_t>(w & 3) << 2);
 }
 // The KB words of group g of the tile's block and its lookahead word (the
 // next word, or word 0 of the block for group 0).
 template <int KB>
 __device__ __forceinline__ void tile_group_words(uint32_t rb, uint32_t r7, int g, uint32_t (&w)[KB + 1]) {
     const int w0 = (kGroupsPerBlock - 1 - g) * KB;
-    if constexpr (KB == 4) {
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(code_word_addr(rb, r7, w0)));
+    if constexpr (KB == 4 || KB == 8) {
+        // 16-byte aligned chunks inside one box
+#pragma unroll
+        for (int q = 0; q < KB; q += 4)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[q]), "=r"(w[q + 1]), "=r"(w[q + 2]), "=r"(w[q + 3])
+                         : "r"(code_word_addr(rb, r7, w0 + q)));
     } else if constexpr (KB == 2) {
         asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(code_word_addr(rb, r7, w0)));
     } else {
@@ -562,11 +576,13 @@ __device__ __forceinline__ void tile_group_words(uint32_t rb, uint32_t r7, int g
     w[KB] = lds32(code_word_addr(rb, r7, (w0 + KB) % (kGroupsPerBlock * KB)));
 }
 
-template <int KB, int NB, bool TAB>
+template <int KB, int NB, bool TAB, int LL>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out, int M, int K, int N,
-                const __grid_constant__ CUtensorMap x_map, const __grid_constant__ CUtensorMap code_map) {
-    using S = TcaShape<NB, TAB>;
+                uint32_t lmask, const __grid_constant__ CUtensorMap x_map,
+                const __grid_constant__ CUtensorMap code_map) {
+    using S = TcaShape<NB, TAB, KB>;
+    constexpr int kBoxes = code_boxes(KB);
     constexpr int kS = S::kStages;
     constexpr int kBBytes = S::kBBytes;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -608,9 +624,12 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
         // L2 prefetches of the first code tiles (no data reaches the CTA
         // before the wait for the previous grid; L2 cannot hold a stale line)
         for (int b = 0; b < kCodeSlots && b < nblocks; ++b)
-            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                         :: "l"(reinterpret_cast<uint64_t>(&code_map)), "r"(b * kGroupsPerBlock * KB), "r"(n0)
-                         : "memory");
+#pragma unroll
+            for (int q = 0; q < kBoxes; ++q)
+                asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                             :: "l"(reinterpret_cast<uint64_t>(&code_map)),
+                                "r"(b * kGroupsPerBlock * KB + q * kCodeTileWords), "r"(n0)
+                             : "memory");
     }
     griddep_wait();
 
@@ -645,7 +664,7 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
             if (!code_ready) alive = mbar_wait(bar_code + 8 * c, static_cast<uint32_t>(cpar));
             if (alive && !slot_ready) alive = mbar_wait(bar_empty + 8 * (se + 1), static_cast<uint32_t>(spar));
             if (!alive) break;
-            const uint32_t rb = rb0 + static_cast<uint32_t>(c * kCodeTileBytes);
+            const uint32_t rb = rb0 + static_cast<uint32_t>(c * S::kCodeBytes);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t w[KB + 1];
@@ -658,7 +677,8 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
                         v.x = quotient_lookup(group_window<KB, kL>(w, 2 * jp), lane_tbl);
                         v.y = quotient_lookup(group_window<KB, kL>(w, 2 * jp + 1), lane_tbl);
                     } else {
-                        v = window_value2(group_window<KB, kL>(w, 2 * jp), group_window<KB, kL>(w, 2 * jp + 1));
+                        v = window_value2(group_window<KB, LL>(w, 2 * jp, lmask),
+                                          group_window<KB, LL>(w, 2 * jp + 1, lmask));
                     }
                     const float2 ws = __fmul2_rn(v, s2);
                     packed[jp] = pack_bf16x2(ws.x, ws.y);
@@ -726,9 +746,11 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
             int code_next = 0;
             auto issue_code = [&](int b) {
                 const int cs = b % kCodeSlots;
-                mbar_arrive_expect_tx(bar_code + 8 * cs, static_cast<uint32_t>(kCodeTileBytes));
-                tma_load_2d(sbase + S::kOffCode + cs * kCodeTileBytes, &code_map, b * kGroupsPerBlock * KB, n0,
-                            bar_code + 8 * cs);
+                mbar_arrive_expect_tx(bar_code + 8 * cs, static_cast<uint32_t>(S::kCodeBytes));
+#pragma unroll
+                for (int q = 0; q < kBoxes; ++q)
+                    tma_load_2d(sbase + S::kOffCode + cs * S::kCodeBytes + q * kCodeTileBytes, &code_map,
+                                b * kGroupsPerBlock * KB + q * kCodeTileWords, n0, bar_code + 8 * cs);
             };
             for (; code_next < kCodeSlots && code_next < nblocks; ++code_next) issue_code(code_next);
             int issued = 0;
@@ -885,11 +907,12 @@ bool make_code_map(CUtensorMap* map, const uint32_t* codes, int N, int row_words
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KB, int NB, bool TAB>
+template <int KB, int NB, bool TAB, int LL>
 int launch_tca_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
-                      uint16_t* out, cudaStream_t stream) {
+                      uint32_t lmask, uint16_t* out, cudaStream_t stream) {
+    using S = TcaShape<NB, TAB, KB>;
     static std::atomic<unsigned long long> opted{0};
-    if (!smem_opt_in(gemm_tca_kernel<KB, NB, TAB>, TcaShape<NB, TAB>::kSmemBytes, opted)) return -5;
+    if (!smem_opt_in(gemm_tca_kernel<KB, NB, TAB, LL>, S::kSmemBytes, opted)) return -5;
     const int grid = (N + kTcRows - 1) / kTcRows;
     CUtensorMap cmap;
     if (!make_code_map(&cmap, codes, N, K / 32 * KB)) return -5;
@@ -898,26 +921,28 @@ int launch_tca_chunks(const uint16_t* x, const uint32_t* codes, const uint16_t* 
         const int mc = (M - m0) < NB ? (M - m0) : NB;
         CUtensorMap map;
         if (!make_x_map(&map, x + static_cast<size_t>(m0) * K, mc, K, tc_box_rows(mc, NB))) return -5;
-        const cudaError_t e = launch_programmatic(gemm_tca_kernel<KB, NB, TAB>, static_cast<unsigned>(grid),
-                                                  static_cast<unsigned>(kTcThreads), TcaShape<NB, TAB>::kSmemBytes,
-                                                  stream, scales, out + static_cast<size_t>(m0) * N, mc, K, N, map,
-                                                  cmap);
+        const cudaError_t e = launch_programmatic(gemm_tca_kernel<KB, NB, TAB, LL>, static_cast<unsigned>(grid),
+                                                  static_cast<unsigned>(kTcThreads), S::kSmemBytes, stream, scales,
+                                                  out + static_cast<size_t>(m0) * N, mc, K, N, lmask, map, cmap);
         if (e != cudaSuccess) return -5;
     }
     return 0;
 }
 
-template <int KB>
+// LL = kL (k in {2, 3, 4}, 12-bit windows: the quotient table at NB = 64) or 0
+// (the window width from L at run time, the computed quotient).
+template <int KB, int LL>
 int launch_tca_instance(const uint16_t* x, const uint32_t* codes, const uint16_t* scales, int M, int K, int N,
-                        uint16_t* out, cudaStream_t stream) {
-    if (M <= 64) return launch_tca_chunks<KB, 64, true>(x, codes, scales, M, K, N, out, stream);
-    if (M <= 128) return launch_tca_chunks<KB, 128, false>(x, codes, scales, M, K, N, out, stream);
+                        int L, uint16_t* out, cudaStream_t stream) {
+    const uint32_t lmask = (1u << L) - 1u;
+    if (M <= 64) return launch_tca_chunks<KB, 64, LL == kL, LL>(x, codes, scales, M, K, N, lmask, out, stream);
+    if (M <= 128) return launch_tca_chunks<KB, 128, false, LL>(x, codes, scales, M, K, N, lmask, out, stream);
     // 256 activation rows: 64 KB activation tiles leave shared memory for two
     // stages only, and with two tensor-memory A slots the decode of a pair
     // cannot start before the previous pair's MMAs are done (M = 256:
     // 56.3 us against 43.4 for the shared-memory-A kernel, which overlaps them
     // within its two stages), so these chunks take the shared-memory-A kernel
-    return launch_tc_chunks<KB, 256, kL>(x, codes, scales, M, K, N, (1u << kL) - 1u, out, stream);
+    return launch_tc_chunks<KB, 256, LL>(x, codes, scales, M, K, N, lmask, out, stream);
 }
 
 // The MMA's N follows M: 64 for M <= 64, 128 for M <= 128, else 256.  Above
@@ -941,20 +966,22 @@ int launch_gemm_tc(const uint16_t* x, const uint32_t* codes, const uint16_t* sca
                    int L, uint16_t* out, cudaStream_t stream) {
     if (fast_geometry(k, L)) {
         switch (k) {
-            case 2: return launch_tca_instance<2>(x, codes, scales, M, K, N, out, stream);
-            case 3: return launch_tca_instance<3>(x, codes, scales, M, K, N, out, stream);
-            default: return launch_tca_instance<4>(x, codes, scales, M, K, N, out, stream);
+            case 2: return launch_tca_instance<2, kL>(x, codes, scales, M, K, N, L, out, stream);
+            case 3: return launch_tca_instance<3, kL>(x, codes, scales, M, K, N, L, out, stream);
+            default: return launch_tca_instance<4, kL>(x, codes, scales, M, K, N, L, out, stream);
         }
     }
     switch (k) {
+        // k = 1: a block's 8 words are a quarter of a code box, and the
+        // shared-memory-A kernel measured faster (30.8 against 31.9 us at M = 64)
         case 1: return launch_tc_instance<1, 0>(x, codes, scales, M, K, N, L, out, stream);
-        case 2: return launch_tc_instance<2, 0>(x, codes, scales, M, K, N, L, out, stream);
-        case 3: return launch_tc_instance<3, 0>(x, codes, scales, M, K, N, L, out, stream);
-        case 4: return launch_tc_instance<4, 0>(x, codes, scales, M, K, N, L, out, stream);
-        case 5: return launch_tc_instance<5, 0>(x, codes, scales, M, K, N, L, out, stream);
-        case 6: return launch_tc_instance<6, 0>(x, codes, scales, M, K, N, L, out, stream);
-        case 7: return launch_tc_instance<7, 0>(x, codes, scales, M, K, N, L, out, stream);
-        case 8: return launch_tc_instance<8, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 2: return launch_tca_instance<2, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 3: return launch_tca_instance<3, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 4: return launch_tca_instance<4, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 5: return launch_tca_instance<5, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 6: return launch_tca_instance<6, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 7: return launch_tca_instance<7, 0>(x, codes, scales, M, K, N, L, out, stream);
+        case 8: return launch_tca_instance<8, 0>(x, codes, scales, M, K, N, L, out, stream);
         default: return -3;
     }
 }
