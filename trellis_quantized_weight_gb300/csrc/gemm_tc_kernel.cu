@@ -17,25 +17,25 @@
 // one TMA warp and one MMA warp (one thread issues the 8 tcgen05.mma, K = 16
 // each, of a 128-k stage and commits them to the stage's "empty" barrier).
 // Two kernels:
-//   * gemm_tca_kernel, k = 2 .. 8 with NB = 64 or 128: the TMA thread loads
-//     each block's code words (one or two 128-byte boxes a row) for the CTA's
-//     128 rows into shared memory next to the activation tiles; decode warp w
-//     takes weight rows 32*(w%4) .. +31 (one row a lane) and group w/4 of each
-//     stage, reads its words from shared memory and writes the decoded bf16
-//     values straight into tensor memory (tcgen05.st), where the MMA takes A
-//     from.
-//   * gemm_tc_kernel, NB = 256 (where 64 KB activation tiles leave room for
-//     two stages only) and k = 1: decode warps load their code words from
-//     global memory and write the A tile to shared memory in the K-major
-//     128-byte-swizzled layout (two k-blocks of 64 k, each row of a k-block
-//     128 bytes, and inside every 8-row (1 KB) atom the 16-byte chunk c of row
-//     r stored at chunk c ^ r), published to the tensor cores by a proxy fence.
+//   * gemm_tca_kernel, k = 2 .. 8: the TMA thread loads each block's code
+//     words (one or two 128-byte boxes a row) for the CTA's 128 rows into
+//     shared memory next to the activation tiles; decode warp w takes weight
+//     rows 32*(w%4) .. +31 (one row a lane) and group w/4 of each stage, reads
+//     its words from shared memory and writes the decoded bf16 values straight
+//     into tensor memory (tcgen05.st), where the MMA takes A from.  Four A
+//     slots in tensor memory; four or six activation slots, two at NB = 256.
+//   * gemm_tc_kernel, k = 1 (a block's 8 words are a quarter of a code box):
+//     decode warps load their code words from global memory and write the A
+//     tile to shared memory in the K-major 128-byte-swizzled layout (two
+//     k-blocks of 64 k, each row of a k-block 128 bytes, and inside every 8-row
+//     (1 KB) atom the 16-byte chunk c of row r stored at chunk c ^ r),
+//     published to the tensor cores by a proxy fence.
 // The quotient: with NB = 64 and the page's geometry (k in {2, 3, 4}, 12-bit
-// windows) the tensor-memory kernel reads it from the
-// per-lane shared-memory table of the CUDA-core kernel (one dp4a address and
-// one load a window, indexed by the hash's byte sum; trellis_device.cuh), which
-// its freed shared memory now holds; otherwise it is computed on the FMA pipe
-// (two-part reciprocal, two windows per f32x2 instruction).  In both kernels
+// windows) the tensor-memory kernel reads it from the per-lane shared-memory
+// table of the CUDA-core kernel (one dp4a address and one load a window,
+// indexed by the hash's byte sum; trellis_device.cuh), which its freed shared
+// memory holds; otherwise it is computed on the FMA pipe (two-part
+// reciprocal, two windows per f32x2 instruction).  In both kernels
 // the TMA warp loads each stage's activation tile with two 2-D tensor copies
 // (one per k-block, 128-byte rows, swizzled by the TMA into the MMA's layout;
 // the box covers the chunk's rows rounded up to 8, and rows beyond it only feed
@@ -516,22 +516,26 @@ __host__ __device__ constexpr int code_boxes(int kb) {
 // where the table, three code slots and four activation slots fit in 227 KB).
 template <int NB, bool TAB, int KB>
 struct TcaShape {
+    // A slots (tensor memory) and activation slots (shared memory); the
+    // activation ring is shallower at NB = 256, whose tiles are 64 KB
     static constexpr int kStages = TAB ? 4 : (NB == 64 ? 6 : 4);
+    static constexpr int kXStages = NB == 256 ? 2 : kStages;
     static constexpr int kBBytes = NB * kTcStageK * 2;
     static constexpr int kCodeBytes = code_boxes(KB) * kCodeTileBytes;   // one code slot
     static constexpr int kOffB = 0;
-    static constexpr int kOffCode = kOffB + kStages * kBBytes;
+    static constexpr int kOffCode = kOffB + kXStages * kBBytes;
     static constexpr int kOffTable = kOffCode + kCodeSlots * kCodeBytes;
     static constexpr int kOffBar = kOffTable + (TAB ? kQuotientTableBytes : 0);
-    static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarTma = 2 * kStages, kBarCode = 3 * kStages,
-                         kBarDone = 3 * kStages + kCodeSlots;
+    static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarTma = 2 * kStages,
+                         kBarXEmpty = 2 * kStages + kXStages, kBarCode = 2 * kStages + 2 * kXStages,
+                         kBarDone = 2 * kStages + 2 * kXStages + kCodeSlots;
     static constexpr int kOffTaddr = kOffBar + (kBarDone + 1) * 8;
     static constexpr int kSmemBytes = kOffTaddr + 16 + 1024;
     static constexpr int kAColBase = NB;          // accumulator: columns [0, NB)
     static constexpr int kTmemCols = 512;
-    static_assert(NB == 64 || NB == 128, "MMA N of this kernel");
+    static_assert(NB == 64 || NB == 128 || NB == 256, "MMA N");
     static_assert(NB + kStages * 64 <= kTmemCols, "tensor memory columns");
-    static_assert(kStages % 2 == 0 && kStages <= 2 * kCodeSlots, "stage pairs; code slot reuse");
+    static_assert(kStages % 2 == 0 && kXStages <= 2 * kCodeSlots, "stage pairs; code slot reuse");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
     static_assert(!TAB || KB <= 4, "the quotient table serves 12-bit windows of k <= 4");
     static_assert(kOffCode % 1024 == 0 && kBBytes % 1024 == 0 && kCodeBytes % 1024 == 0,
@@ -595,15 +599,21 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
     const uint32_t bar_tma = sbase + S::kOffBar + 8 * S::kBarTma;
     const uint32_t bar_code = sbase + S::kOffBar + 8 * S::kBarCode;
     const uint32_t bar_done = sbase + S::kOffBar + 8 * S::kBarDone;
+    constexpr int kSX = S::kXStages;
+    // with as many activation slots as A slots, one commit frees both
+    const uint32_t bar_xempty = kSX == kS ? bar_empty : sbase + S::kOffBar + 8 * S::kBarXEmpty;
     const int nstages = K / kTcStageK;
     const int nblocks = nstages / 2;
     const int n0 = blockIdx.x * kTcRows;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kS; ++s) {
-            mbar_init(bar_full + 8 * s, kTcDecodeWarps);
-            mbar_init(bar_empty + 8 * s, 1);
-            mbar_init(bar_tma + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, kTcDecodeWarps);   // the decode warps' arrivals
+            mbar_init(bar_empty + 8 * s, 1);               // the MMAs' commit: A slot free
+        }
+        for (int s = 0; s < kSX; ++s) {
+            mbar_init(bar_tma + 8 * s, 1);                 // expect_tx, then the activation bytes
+            if (kSX != kS) mbar_init(bar_xempty + 8 * s, 1);   // the MMAs' commit: activation slot free
         }
         for (int c = 0; c < kCodeSlots; ++c) mbar_init(bar_code + 8 * c, 1);
         mbar_init(bar_done, 1);
@@ -755,8 +765,8 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
             for (; code_next < kCodeSlots && code_next < nblocks; ++code_next) issue_code(code_next);
             int issued = 0;
             for (int i = 0; i < nstages; ++i) {
-                const int s = i % kS;
-                if (i >= kS && !mbar_wait(bar_empty + 8 * s, ((i / kS) + 1) & 1)) break;
+                const int s = i % kSX;
+                if (i >= kSX && !mbar_wait(bar_xempty + 8 * s, ((i / kSX) + 1) & 1)) break;
                 mbar_arrive_expect_tx(bar_tma + 8 * s, static_cast<uint32_t>(2 * rows * kSwRowBytes));
                 const uint32_t dst = sbase + S::kOffB + s * kBBytes;
 #pragma unroll
@@ -764,18 +774,18 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
                     tma_load_2d(dst + kb * (NB * kSwRowBytes), &x_map, i * kTcStageK + kb * kSwK, 0,
                                 bar_tma + 8 * s);
                 issued = i + 1;
-                // The MMAs of stage i - kS are complete (waited above), so the
-                // decode of every stage up to i - kS is too: block p's code
+                // The MMAs of stage i - kSX are complete (waited above), so the
+                // decode of every stage up to i - kSX is too: block p's code
                 // slot (that of block p - kCodeSlots) is free once stage
-                // 2 (p - kCodeSlots) + 1 <= i - kS.
-                if (i >= kS) {
-                    const int lim = ((i - kS - 1) >> 1) + kCodeSlots;
+                // 2 (p - kCodeSlots) + 1 <= i - kSX.
+                if (i >= kSX) {
+                    const int lim = ((i - kSX - 1) >> 1) + kCodeSlots;
                     for (; code_next <= lim && code_next < nblocks; ++code_next) issue_code(code_next);
                 }
             }
             // every copy issued has landed before the CTA can exit
-            for (int i = issued > kS ? issued - kS : 0; i < issued; ++i)
-                (void)mbar_wait(bar_tma + 8 * (i % kS), (i / kS) & 1);
+            for (int i = issued > kSX ? issued - kSX : 0; i < issued; ++i)
+                (void)mbar_wait(bar_tma + 8 * (i % kSX), (i / kSX) & 1);
             for (int b = code_next > kCodeSlots ? code_next - kCodeSlots : 0; b < code_next; ++b)
                 (void)mbar_wait(bar_code + 8 * (b % kCodeSlots), (b / kCodeSlots) & 1);
         }
@@ -785,9 +795,9 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
             const uint64_t db0 = smem_desc(sbase + S::kOffB);
             const uint32_t db_hi = static_cast<uint32_t>(db0 >> 32);
             auto issue_stage = [&](int i) {
-                const int s = i % kS;
+                const int s = i % kS, sx = i % kSX;
                 const uint32_t ta_s = taddr + static_cast<uint32_t>(S::kAColBase + 64 * s);
-                const uint32_t db_s = static_cast<uint32_t>(db0) + static_cast<uint32_t>(s * (kBBytes >> 4));
+                const uint32_t db_s = static_cast<uint32_t>(db0) + static_cast<uint32_t>(sx * (kBBytes >> 4));
 #pragma unroll
                 for (int kk = 0; kk < kTcStageK / 16; ++kk) {
                     const int kb = kk / (kSwK / 16), ks = kk % (kSwK / 16);
@@ -797,6 +807,7 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
                                 (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar_empty + 8 * s);
+                if constexpr (kSX != kS) mma_commit(bar_xempty + 8 * sx);
             };
             // Stages are published in pairs (the last pair stage by stage), so
             // the four barrier probes of a pair are issued back to back (their
@@ -806,16 +817,16 @@ gemm_tca_kernel(const uint16_t* __restrict__ scales, uint16_t* __restrict__ out,
                 bool ready[4];
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
-                    const int t = i + p, s = t % kS, par = (t / kS) & 1;
-                    ready[2 * p] = mbar_try_wait(bar_tma + 8 * s, par);
-                    ready[2 * p + 1] = mbar_try_wait(bar_full + 8 * s, par);
+                    const int t = i + p;
+                    ready[2 * p] = mbar_try_wait(bar_tma + 8 * (t % kSX), (t / kSX) & 1);
+                    ready[2 * p + 1] = mbar_try_wait(bar_full + 8 * (t % kS), (t / kS) & 1);
                 }
                 bool ok = true;
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
-                    const int t = i + p, s = t % kS, par = (t / kS) & 1;
-                    if (ok && !ready[2 * p]) ok = mbar_wait(bar_tma + 8 * s, par);
-                    if (ok && !ready[2 * p + 1]) ok = mbar_wait(bar_full + 8 * s, par);
+                    const int t = i + p;
+                    if (ok && !ready[2 * p]) ok = mbar_wait(bar_tma + 8 * (t % kSX), (t / kSX) & 1);
+                    if (ok && !ready[2 * p + 1]) ok = mbar_wait(bar_full + 8 * (t % kS), (t / kS) & 1);
                     if (!ok) break;
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     issue_stage(t);
@@ -937,12 +948,7 @@ int launch_tca_instance(const uint16_t* x, const uint32_t* codes, const uint16_t
     const uint32_t lmask = (1u << L) - 1u;
     if (M <= 64) return launch_tca_chunks<KB, 64, LL == kL, LL>(x, codes, scales, M, K, N, lmask, out, stream);
     if (M <= 128) return launch_tca_chunks<KB, 128, false, LL>(x, codes, scales, M, K, N, lmask, out, stream);
-    // 256 activation rows: 64 KB activation tiles leave shared memory for two
-    // stages only, and with two tensor-memory A slots the decode of a pair
-    // cannot start before the previous pair's MMAs are done (M = 256:
-    // 56.3 us against 43.4 for the shared-memory-A kernel, which overlaps them
-    // within its two stages), so these chunks take the shared-memory-A kernel
-    return launch_tc_chunks<KB, 256, LL>(x, codes, scales, M, K, N, lmask, out, stream);
+    return launch_tca_chunks<KB, 256, false, LL>(x, codes, scales, M, K, N, lmask, out, stream);
 }
 
 // The MMA's N follows M: 64 for M <= 64, 128 for M <= 128, else 256.  Above
