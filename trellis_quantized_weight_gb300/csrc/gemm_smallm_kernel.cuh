@@ -42,8 +42,12 @@
 //    byte sum into a float and the two-op quotient (trellis_device.cuh), or one
 //    dp4a that turns the hash into the address of the quotient in a per-lane
 //    shared-memory table (one conflict-free load).  Then a packed f32x2 scale
-//    multiply, a bf16 round that keeps fp32 format, and MM packed f32x2 FMAs
-//    per weight pair and row (two k at once).
+//    multiply, a bf16 round that keeps fp32 format, and the packed f32x2 FMAs
+//    of the multiply: either MM per weight pair and row (two k at once, x
+//    staged as [group][m][k]), or, for the shapes marked MP, ceil(MM/2) per
+//    weight and row (two activation rows at once with the weight in both
+//    halves, which the FMA takes from one register; x staged as
+//    [group][k][m]): half the fp32 sums a lane holds.
 #pragma once
 
 #include <cstdint>
@@ -93,19 +97,24 @@ struct SmallMPlan {
 //   TWO    two weight matrices sharing x (gate and up); single-matrix kernels
 //          carry none of the row mapping
 template <int MM_, int R_, int WARPS_, bool LUT_, int OCC_ = 1, int UB_ = 2, bool GM_ = false, bool ET_ = false,
-          bool TWO_ = false>
+          bool TWO_ = false, bool MP_ = false>
 struct SmallMCfg {
     static constexpr int MM = MM_;
     static constexpr int R = R_;
     static constexpr int WARPS = WARPS_;
     static constexpr bool LUT = LUT_;
     static constexpr int OCC = OCC_;                              // CTAs per SM
-    static constexpr int XG = 32 * MM + 4;                        // floats per staged (block, group)
+    // MP: each f32x2 FMA takes a pair of activation rows (m, m+1) and one
+    // weight in both halves; else a pair of k for one activation row
+    static constexpr bool MP = MP_;
+    static constexpr int MMP = MP ? (MM + 1) / 2 * 2 : MM;        // activation rows staged (even for MP)
+    static constexpr int XG = 32 * MMP + 4;                       // floats per staged (block, group)
     static constexpr int XS_UNIT = 8 * XG;                        // floats of staged x per block
     static constexpr int TABLE_BYTES = LUT ? kQuotientTableBytes : 0;
     static constexpr int ROWS_PER_TILE = 4 * R;
     static constexpr int NT = WARPS * 32;
     static constexpr int XV = MM * 32;                            // 8-element x vectors per block
+    static constexpr int NACC = MP ? MMP / 2 : MM;                // f32x2 sums per row a lane holds
     static constexpr int XPT = (XV + NT - 1) / NT;                // x vectors staged per thread per block
     static constexpr int UB = UB_;                                // blocks per CTA barrier
     static constexpr int RING = 2 * UB;                           // x ring slots
@@ -123,12 +132,20 @@ struct SmallMCfg {
 // faster; M = 9 and 10 measured the same or faster at 12.
 template <int MM>
 struct SmallMDefault {
-    static constexpr int WARPS = (MM <= 2) ? 16 : (MM <= 10 ? 12 : 8);
+    // Pairs of activation rows per f32x2 FMA (MP) for M = 11 .. 16 except 15:
+    // half the sums a lane holds, so 12 warps fit (A/B on one GB300, K = 5120,
+    // N = 17408, k = 4; M = 11 at k = 3): M = 11 69.5 -> 68.2 us, 12 69.6 ->
+    // 64.2, 13 72.1 -> 71.5, 14 77.2 -> 72.7 (8 warps), 16 82.0 -> 79.4.  At
+    // M = 15 the padding row and 52 bytes of spills at 12 warps made it slower
+    // (79.8, and 81.8 at 8 warps, against 78.8), so M = 15 keeps k-pairs.
+    static constexpr bool MPD = MM >= 11 && MM != 15;
+    static constexpr int KWARPS = (MM <= 2) ? 16 : (MM <= 10 ? 12 : 8);   // with k-pairs
+    static constexpr int WARPS = MPD ? (MM == 14 ? 8 : 12) : KWARPS;
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
     static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
     static constexpr bool ET = MM >= 12;
-    using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET>;
-    using two = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, true>;   // gate and up
+    using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, false, MPD>;
+    using two = SmallMCfg<MM, 3, KWARPS, true, 1, UB, GM, ET, true>;   // gate and up
     // any other (k, L): the quotient table only holds the byte sums that
     // 12-bit windows reach, so these compute the quotient, which needs more
     // registers: 8 warps (255 registers a thread) from M = 6 up, and 2 rows a
@@ -257,7 +274,6 @@ __device__ __forceinline__ void x_block_store(float* slot, int tid, const uint4 
         const int e = tid + i * C::NT;
         if (e < C::XV) {
             const int m = e >> 5, c8 = e & 31;
-            float* dst = slot + (c8 >> 2) * C::XG + m * 32 + (c8 & 3) * 8;
             const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
             float f[8];
 #pragma unroll
@@ -265,8 +281,16 @@ __device__ __forceinline__ void x_block_store(float* slot, int tid, const uint4 
                 f[2 * h] = __uint_as_float(u[h] << 16);
                 f[2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
             }
-            *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
-            *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
+            if constexpr (C::MP) {
+                // [group][k][m]: the activation rows of one k are adjacent
+                float* dst = slot + (c8 >> 2) * C::XG + ((c8 & 3) * 8) * C::MMP + m;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dst[j * C::MMP] = f[j];
+            } else {
+                float* dst = slot + (c8 >> 2) * C::XG + m * 32 + (c8 & 3) * 8;
+                *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(f[4], f[5], f[6], f[7]);
+            }
         }
     }
 }
@@ -395,7 +419,8 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     bool ok[R];
     float2 s2[R];
     const uint32_t* rp[R];
-    float2 acc[R][MM];
+    constexpr int NACC = C::NACC;
+    float2 acc[R][NACC];
     uint32_t cw[R][KB];
     int tg = -1, row0 = 0, tile = 0, b_first = 0;
     bool live = false;
@@ -426,7 +451,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             s2[r] = make_float2(sr, sr);
             rp[r] = rs.codes + static_cast<size_t>(ok[r] ? nl : 0) * p.row_words;
 #pragma unroll
-            for (int m = 0; m < MM; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
+            for (int m = 0; m < NACC; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
         }
         if (live && !prefetched) load_block_group<KB, R>(rp, ok, b, lg, cw);
     };
@@ -455,6 +480,13 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                          :: "l"(x + static_cast<size_t>(tid >> 2) * p.K + b * 256 + (tid & 3) * 64));
     }
     if constexpr (C::LUT) build_quotient_table(reinterpret_cast<float*>(smem_raw), tid, NT);
+    if constexpr (C::MP && C::MMP != MM) {
+        // the padding activation row (m = M) of every ring slot stays zero
+        for (int i = tid; i < C::RING * 8 * 32; i += NT) {
+            const int slot_i = i >> 8, gk = i & 255;
+            xs[slot_i * XS_UNIT + (gk >> 5) * XG + (gk & 31) * C::MMP + MM] = 0.0f;
+        }
+    }
     griddep_wait();
     if (nunits > 0) begin_segment(false);
     {
@@ -564,19 +596,11 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 }
             }
             const float* xq = xs + ring * XS_UNIT + g * XG;
+            if constexpr (C::MP) {
 #pragma unroll
-            for (int pq = 0; pq < 8; ++pq) {
-                // k-pairs 2pq and 2pq+1 of the group: x[m][4pq .. 4pq+3]
-                float2 xa[MM], xb[MM];
-#pragma unroll
-                for (int m = 0; m < MM; ++m) {
-                    const float4 t = *reinterpret_cast<const float4*>(xq + m * 32 + 4 * pq);
-                    xa[m] = make_float2(t.x, t.y);
-                    xb[m] = make_float2(t.z, t.w);
-                }
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int pp = 2 * pq + half;
+                for (int pp = 0; pp < 16; ++pp) {
+                    // weights of k-pair pp (k = 2pp, 2pp+1 of the group) for each row
+                    float2 wv[R];
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         float2 v;
@@ -589,10 +613,64 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                                               group_window<KB, LL>(w[r], 2 * pp + 1, p.lmask));
                         }
                         const float2 ws = __fmul2_rn(v, s2[r]);
-                        const float2 wv = make_float2(round_bf16_as_f32(ws.x), round_bf16_as_f32(ws.y));
+                        wv[r] = make_float2(round_bf16_as_f32(ws.x), round_bf16_as_f32(ws.y));
+                    }
 #pragma unroll
-                        for (int m = 0; m < MM; ++m)
-                            acc[r][m] = __ffma2_rn(wv, half ? xb[m] : xa[m], acc[r][m]);
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const float* xk = xq + (2 * pp + kk) * C::MMP;
+#pragma unroll
+                        for (int q = 0; q < C::MMP / 4; ++q) {
+                            const float4 t = *reinterpret_cast<const float4*>(xk + 4 * q);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                const float wk = kk ? wv[r].y : wv[r].x;
+                                acc[r][2 * q] = __ffma2_rn(make_float2(wk, wk), make_float2(t.x, t.y), acc[r][2 * q]);
+                                if (2 * q + 1 < NACC)
+                                    acc[r][2 * q + 1] =
+                                        __ffma2_rn(make_float2(wk, wk), make_float2(t.z, t.w), acc[r][2 * q + 1]);
+                            }
+                        }
+                        if constexpr (C::MMP % 4 != 0) {
+                            const float2 t2 = *reinterpret_cast<const float2*>(xk + C::MMP - 2);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) {
+                                const float wk = kk ? wv[r].y : wv[r].x;
+                                acc[r][NACC - 1] = __ffma2_rn(make_float2(wk, wk), t2, acc[r][NACC - 1]);
+                            }
+                        }
+                    }
+                }
+            } else {
+    #pragma unroll
+                for (int pq = 0; pq < 8; ++pq) {
+                    // k-pairs 2pq and 2pq+1 of the group: x[m][4pq .. 4pq+3]
+                    float2 xa[MM], xb[MM];
+    #pragma unroll
+                    for (int m = 0; m < MM; ++m) {
+                        const float4 t = *reinterpret_cast<const float4*>(xq + m * 32 + 4 * pq);
+                        xa[m] = make_float2(t.x, t.y);
+                        xb[m] = make_float2(t.z, t.w);
+                    }
+    #pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int pp = 2 * pq + half;
+    #pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            float2 v;
+                            if constexpr (C::LUT) {
+                                static_assert(LL == kL, "the quotient table covers 12-bit windows only");
+                                v.x = quotient_lookup(group_window<KB, LL>(w[r], 2 * pp), lane_tbl);
+                                v.y = quotient_lookup(group_window<KB, LL>(w[r], 2 * pp + 1), lane_tbl);
+                            } else {
+                                v = window_value2(group_window<KB, LL>(w[r], 2 * pp, p.lmask),
+                                                  group_window<KB, LL>(w[r], 2 * pp + 1, p.lmask));
+                            }
+                            const float2 ws = __fmul2_rn(v, s2[r]);
+                            const float2 wv = make_float2(round_bf16_as_f32(ws.x), round_bf16_as_f32(ws.y));
+    #pragma unroll
+                            for (int m = 0; m < MM; ++m)
+                                acc[r][m] = __ffma2_rn(wv, half ? xb[m] : xa[m], acc[r][m]);
+                        }
                     }
                 }
             }
@@ -613,7 +691,11 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             float v[NV];
 #pragma unroll
             for (int i = 0; i < NV; ++i)
-                v[i] = (i < R * MM) ? __fadd_rn(acc[i / MM][i % MM].x, acc[i / MM][i % MM].y) : 0.0f;
+                if constexpr (C::MP)
+                    v[i] = (i < R * MM) ? ((i % MM) & 1 ? acc[i / MM][(i % MM) >> 1].y : acc[i / MM][(i % MM) >> 1].x)
+                                        : 0.0f;
+                else
+                    v[i] = (i < R * MM) ? __fadd_rn(acc[i / MM][i % MM].x, acc[i / MM][i % MM].y) : 0.0f;
             int vbase = 0;
 #pragma unroll
             for (int step = 0; step < 3; ++step) {
