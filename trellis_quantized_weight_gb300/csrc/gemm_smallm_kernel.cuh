@@ -44,10 +44,10 @@
 //    shared-memory table (one conflict-free load).  Then a packed f32x2 scale
 //    multiply, a bf16 round that keeps fp32 format, and the packed f32x2 FMAs
 //    of the multiply: either MM per weight pair and row (two k at once, x
-//    staged as [group][m][k]), or, for the shapes marked MP, ceil(MM/2) per
-//    weight and row (two activation rows at once with the weight in both
-//    halves, which the FMA takes from one register; x staged as
-//    [group][k][m]): half the fp32 sums a lane holds.
+//    staged as [group][m][k]), or, for the shapes marked MP, MM/2 per weight
+//    and row (two activation rows at once with the weight in both halves,
+//    which the FMA takes from one register; an odd MM's last row by a scalar
+//    FMA; x staged as [group][k][m]): half the fp32 sums a lane holds.
 #pragma once
 
 #include <cstdint>
@@ -114,7 +114,8 @@ struct SmallMCfg {
     static constexpr int ROWS_PER_TILE = 4 * R;
     static constexpr int NT = WARPS * 32;
     static constexpr int XV = MM * 32;                            // 8-element x vectors per block
-    static constexpr int NACC = MP ? MMP / 2 : MM;                // f32x2 sums per row a lane holds
+    static constexpr bool ODD = MP && (MM & 1);                   // the last activation row alone
+    static constexpr int NACC = MP ? MM / 2 : MM;                 // f32x2 sums per row a lane holds
     static constexpr int XPT = (XV + NT - 1) / NT;                // x vectors staged per thread per block
     static constexpr int UB = UB_;                                // blocks per CTA barrier
     static constexpr int RING = 2 * UB;                           // x ring slots
@@ -132,20 +133,23 @@ struct SmallMCfg {
 // faster; M = 9 and 10 measured the same or faster at 12.
 template <int MM>
 struct SmallMDefault {
-    // Pairs of activation rows per f32x2 FMA (MP) for M = 11 .. 16 except 15:
-    // half the sums a lane holds, so 12 warps fit (A/B on one GB300, K = 5120,
-    // N = 17408, k = 4; M = 11 at k = 3): M = 11 69.5 -> 68.2 us, 12 69.6 ->
-    // 64.2, 13 72.1 -> 71.5, 14 77.2 -> 72.7 (8 warps), 16 82.0 -> 79.4.  At
-    // M = 15 the padding row and 52 bytes of spills at 12 warps made it slower
-    // (79.8, and 81.8 at 8 warps, against 78.8), so M = 15 keeps k-pairs.
-    static constexpr bool MPD = MM >= 11 && MM != 15;
+    // Pairs of activation rows per f32x2 FMA (MP) for M = 11 .. 16, an odd M's
+    // last row on its own (a scalar FMA): half the sums a lane holds, so 12
+    // warps fit (A/B on one GB300, K = 5120, N = 17408, k = 4; M = 11 at
+    // k = 3): M = 11 69.5 -> 67.9 us, 12 69.6 -> 64.2, 13 72.1 -> 69.5,
+    // 14 77.2 -> 72.7 (8 warps), 15 78.7 -> 76.7, 16 82.0 -> 79.4.
+    static constexpr bool MPD = MM >= 11;
     static constexpr int KWARPS = (MM <= 2) ? 16 : (MM <= 10 ? 12 : 8);   // with k-pairs
     static constexpr int WARPS = MPD ? (MM == 14 ? 8 : 12) : KWARPS;
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
     static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
-    static constexpr bool ET = MM >= 12;
+    // early tickets for M >= 12 at 8 warps; off at 12 (M = 12 64.3 -> 63.1 us,
+    // 13 69.6 -> 68.7, 15 76.7 -> 75.7, 16 79.5 -> 78.9; M = 14 at 8 warps
+    // 72.7 with them, 76.7 without)
+    static constexpr bool ET = MM >= 12 && WARPS == 8;
+    static constexpr bool KET = MM >= 12;   // with k-pairs (8 warps)
     using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, false, MPD>;
-    using two = SmallMCfg<MM, 3, KWARPS, true, 1, UB, GM, ET, true>;   // gate and up
+    using two = SmallMCfg<MM, 3, KWARPS, true, 1, UB, GM, KET, true>;   // gate and up
     // any other (k, L): the quotient table only holds the byte sums that
     // 12-bit windows reach, so these compute the quotient, which needs more
     // registers: 8 warps (255 registers a thread) from M = 6 up, and 2 rows a
@@ -157,7 +161,7 @@ struct SmallMDefault {
         return ((MM == 15 && kb == 8) || (MM == 16 && (kb == 4 || kb == 6 || kb == 7))) ? 2 : 3;
     }
     template <int KB>
-    using general = SmallMCfg<MM, general_rows(KB), GWARPS, false, 1, UB, GM, ET>;
+    using general = SmallMCfg<MM, general_rows(KB), GWARPS, false, 1, UB, GM, KET>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
 
@@ -421,6 +425,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     const uint32_t* rp[R];
     constexpr int NACC = C::NACC;
     float2 acc[R][NACC];
+    float acc1[R];   // the last activation row when MM is odd (MP)
     uint32_t cw[R][KB];
     int tg = -1, row0 = 0, tile = 0, b_first = 0;
     bool live = false;
@@ -452,6 +457,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             rp[r] = rs.codes + static_cast<size_t>(ok[r] ? nl : 0) * p.row_words;
 #pragma unroll
             for (int m = 0; m < NACC; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
+            acc1[r] = 0.0f;
         }
         if (live && !prefetched) load_block_group<KB, R>(rp, ok, b, lg, cw);
     };
@@ -624,10 +630,16 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 #pragma unroll
                             for (int r = 0; r < R; ++r) {
                                 const float wk = kk ? wv[r].y : wv[r].x;
-                                acc[r][2 * q] = __ffma2_rn(make_float2(wk, wk), make_float2(t.x, t.y), acc[r][2 * q]);
+                                if (2 * q < NACC)
+                                    acc[r][2 * q] =
+                                        __ffma2_rn(make_float2(wk, wk), make_float2(t.x, t.y), acc[r][2 * q]);
+                                else if (C::ODD && 4 * q == MM - 1)
+                                    acc1[r] = __fmaf_rn(wk, t.x, acc1[r]);
                                 if (2 * q + 1 < NACC)
                                     acc[r][2 * q + 1] =
                                         __ffma2_rn(make_float2(wk, wk), make_float2(t.z, t.w), acc[r][2 * q + 1]);
+                                else if (C::ODD && 4 * q + 2 == MM - 1)
+                                    acc1[r] = __fmaf_rn(wk, t.z, acc1[r]);
                             }
                         }
                         if constexpr (C::MMP % 4 != 0) {
@@ -635,7 +647,10 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 #pragma unroll
                             for (int r = 0; r < R; ++r) {
                                 const float wk = kk ? wv[r].y : wv[r].x;
-                                acc[r][NACC - 1] = __ffma2_rn(make_float2(wk, wk), t2, acc[r][NACC - 1]);
+                                if constexpr (C::ODD)
+                                    acc1[r] = __fmaf_rn(wk, t2.x, acc1[r]);
+                                else
+                                    acc[r][NACC - 1] = __ffma2_rn(make_float2(wk, wk), t2, acc[r][NACC - 1]);
                             }
                         }
                     }
@@ -692,7 +707,9 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 #pragma unroll
             for (int i = 0; i < NV; ++i)
                 if constexpr (C::MP)
-                    v[i] = (i < R * MM) ? ((i % MM) & 1 ? acc[i / MM][(i % MM) >> 1].y : acc[i / MM][(i % MM) >> 1].x)
+                    v[i] = (i < R * MM) ? ((C::ODD && i % MM == MM - 1) ? acc1[i / MM]
+                                           : ((i % MM) & 1 ? acc[i / MM][(i % MM) >> 1].y
+                                                           : acc[i / MM][(i % MM) >> 1].x))
                                         : 0.0f;
                 else
                     v[i] = (i < R * MM) ? __fadd_rn(acc[i / MM][i % MM].x, acc[i / MM][i % MM].y) : 0.0f;
