@@ -155,6 +155,19 @@ def test_every_accepted_geometry_fits_the_fixed_scratch(lib):
     assert 0 < largest <= SCRATCH_LIMIT
 
 
+def test_every_accepted_geometry_fits_trellis_gemm_scratch(lib):
+    """The same for trellis_gemm's 4 MiB static scratch: on this device no
+    single-matrix geometry it accepts needs more, so it never answers
+    TRELLIS_ERR_WORKSPACE here."""
+    from trellis_quantized_weight_gb300 import binding
+    largest = 0
+    for M in range(1, 17):
+        for k, L in [(2, 12), (3, 12), (4, 12), (1, 9), (5, 16), (8, 24)]:
+            for K, N in [(256, 1), (5120, 17408), (17408, 5120), (256, 200000)]:
+                largest = max(largest, binding.gemm_workspace_bytes(M, K, N, k, L))
+    assert 0 < largest <= 4 << 20
+
+
 @pytest.mark.parametrize("M,K,N,k,L", [(6, 1024, 3000, 5, 16), (40, 512, 1000, 1, 9)])
 def test_noalloc_general_geometry(lib, M, K, N, k, L):
     """The no-allocation entry on a geometry outside k in {2,3,4}, L = 12, on

@@ -15,7 +15,9 @@ static size_t ws_bytes_of(int K, int N, int k, const DeviceInfo& dev, bool two) 
 
 template <int MM>
 static size_t ws_bytes_for(int K, int N, int k, int L, const DeviceInfo& dev, bool two) {
-    if (fast_geometry(k, L)) return ws_bytes_of<typename SmallMDefault<MM>::type>(K, N, k, dev, two);
+    if (fast_geometry(k, L))
+        return two ? ws_bytes_of<typename SmallMDefault<MM>::two>(K, N, k, dev, true)
+                   : ws_bytes_of<typename SmallMDefault<MM>::type>(K, N, k, dev, false);
     // other geometries run the two matrices of a pair as two launches, one
     // after the other on the stream, through the same workspace
     switch (k) {

@@ -133,14 +133,18 @@ struct SmallMCfg {
 // faster; M = 9 and 10 measured the same or faster at 12.
 template <int MM>
 struct SmallMDefault {
-    // Pairs of activation rows per f32x2 FMA (MP) for M = 11 .. 16, an odd M's
-    // last row on its own (a scalar FMA): half the sums a lane holds, so 12
-    // warps fit (A/B on one GB300, K = 5120, N = 17408, k = 4; M = 11 at
-    // k = 3): M = 11 69.5 -> 67.9 us, 12 69.6 -> 64.2, 13 72.1 -> 69.5,
-    // 14 77.2 -> 72.7 (8 warps), 15 78.7 -> 76.7, 16 82.0 -> 79.4.
-    static constexpr bool MPD = MM >= 11;
+    // Pairs of activation rows per f32x2 FMA (MP) from M = 3, an odd M's last
+    // row on its own (a scalar FMA): half the sums a lane holds, so more warps
+    // fit.  A/B on one GB300 (K = 5120, N = 17408; k = 2 for M = 5, 6, k = 3
+    // for M = 7 .. 11, else k = 4), us: M = 3 37.3 -> 35.8, 4 40.4 -> 37.7,
+    // 5 42.8 -> 41.2, 6 47.3 -> 43.8, 7 52.3 -> 50.0, 8 54.5 -> 50.3,
+    // 9 59.6 -> 57.2, 10 64.7 -> 58.8 (16 warps); 11 69.5 -> 67.9, 12 69.6 ->
+    // 64.2, 13 72.1 -> 69.5, 15 78.7 -> 76.7, 16 82.0 -> 79.4 (12 warps; 16
+    // spilled and measured slower at M = 11, 12); 14 77.2 -> 72.7 (8 warps).
+    // M = 1, 2 keep k-pairs (a pair of rows would leave half of each FMA idle).
+    static constexpr bool MPD = MM >= 3;
     static constexpr int KWARPS = (MM <= 2) ? 16 : (MM <= 10 ? 12 : 8);   // with k-pairs
-    static constexpr int WARPS = MPD ? (MM == 14 ? 8 : 12) : KWARPS;
+    static constexpr int WARPS = MPD ? (MM <= 10 ? 16 : (MM == 14 ? 8 : 12)) : KWARPS;
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
     static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
     // early tickets for M >= 12 at 8 warps; off at 12 (M = 12 64.3 -> 63.1 us,
