@@ -186,6 +186,23 @@ def test_gemm_gateup(tq, oracle_lib, M, k):
     assert np.all(err <= ulp_bf16_of(ref_act)), f"act: max excess {float((err - ulp_bf16_of(ref_act)).max())}"
 
 
+@pytest.mark.parametrize("M,N,k", [(8, 1300, 3), (15, 870, 4), (5, 1740, 2)])
+def test_gemm_gateup_dead_tile_before_second_matrix(tq, oracle_lib, M, N, k):
+    """A CTA's range runs from the first matrix's last tile-group, where whole
+    tiles lie past N, into the second matrix's first tile-group: the tiles
+    past N request nothing for their next segment, which must then load its
+    own codes and scales (K long enough that CTAs take several units)."""
+    K = 5120
+    x, cg, sg = _inputs(M, K, N, k, seed=2400 + M)
+    _, cu, su = _inputs(M, K, N, k, seed=2500 + M)
+    g, u, a = tq.gemm_gateup(dev_bf16(x), dev_codes(cg), dev_bf16(sg), dev_codes(cu), dev_bf16(su), k,
+                             act=False)
+    for got, codes, scales, what in ((g, cg, sg, "gate"), (u, cu, su, "up")):
+        w = oracle_decode_par(oracle_lib, codes, scales, K, N, k)
+        ref, refabs = oracle_gemm_par(oracle_lib, x, w)
+        assert_gemm_close(host_bits(got), ref, refabs, f"{what} M={M} N={N} k={k}")
+
+
 def test_gemm_gateup_without_activation(tq, oracle_lib):
     """act=False returns no third output; gate and up, over a K long enough to be
     split across CTAs, match the oracle products."""

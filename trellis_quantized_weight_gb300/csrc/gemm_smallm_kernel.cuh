@@ -554,7 +554,12 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 }
         }
 
-        if (seg_start && rel > 0) begin_segment(true);
+        // The next segment's codes and scales were requested during the last
+        // unit of this warp's previous tile only if that tile held rows (a
+        // tile wholly past N skips its work, the request included).  With two
+        // matrices such a tile can end the first matrix and be followed by the
+        // second one's first tile-group in the same CTA, so then load them now.
+        if (seg_start && rel > 0) begin_segment(live);
         // the last unit of a split segment: read its tile's counter (the other
         // contributors have had the whole kernel to take their tickets)
         if (C::ET && rel + 1 == nunits && live && !(b_first == 0 && b + 1 == p.nblocks) && lane == 0)
