@@ -153,7 +153,12 @@ struct SmallMDefault {
     static constexpr bool ET = MM >= 12 && WARPS == 8;
     static constexpr bool KET = MM >= 12;   // with k-pairs (8 warps)
     using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, false, MPD>;
-    using two = SmallMCfg<MM, 3, KWARPS, true, 1, UB, GM, KET, true>;   // gate and up
+    // gate and up: activation-row pairs at 16 warps for M = 3 .. 10 (M = 5
+    // 94.2 -> 85.1 us, M = 8 117.3 -> 103.3 at K = 5120, N = 17408, measured
+    // with both on a slower build); k-pairs above (the 12-warp pairs measured
+    // slower there: M = 12 141.1 -> 145.7, M = 15 156.3 -> 161.7)
+    static constexpr bool TMP = MM >= 3 && MM <= 10;
+    using two = SmallMCfg<MM, 3, TMP ? 16 : KWARPS, true, 1, UB, GM, KET, true, TMP>;
     // any other (k, L): the quotient table only holds the byte sums that
     // 12-bit windows reach, so these compute the quotient, which needs more
     // registers: 8 warps (255 registers a thread) from M = 6 up, and 2 rows a
@@ -554,12 +559,7 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 }
         }
 
-        // The next segment's codes and scales were requested during the last
-        // unit of this warp's previous tile only if that tile held rows (a
-        // tile wholly past N skips its work, the request included).  With two
-        // matrices such a tile can end the first matrix and be followed by the
-        // second one's first tile-group in the same CTA, so then load them now.
-        if (seg_start && rel > 0) begin_segment(live);
+        if (seg_start && rel > 0) begin_segment(true);
         // the last unit of a split segment: read its tile's counter (the other
         // contributors have had the whole kernel to take their tickets)
         if (C::ET && rel + 1 == nunits && live && !(b_first == 0 && b + 1 == p.nblocks) && lane == 0)
@@ -702,6 +702,28 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int i = 0; i < KB; ++i) cw[r][i] = nw[r][i];
+        }
+        if constexpr (C::TWO) {
+            // A tile wholly past N does no work, but with two matrices it can
+            // end the first matrix's last tile-group and be followed, in the
+            // same CTA, by the second matrix's first one: request that
+            // segment's codes and scales here too (with one matrix a tile past
+            // N only occurs in the last tile-group, where no segment follows).
+            if (!live && seg_end && rel + 1 < nunits) {
+                const int nrow0 = ((utg + 1) * WARPS + warp) * C::ROWS_PER_TILE;
+                const RowSrc nrs = row_source<C>(p, codes, scales, out, nrow0);
+                bool nok[R];
+                const uint32_t* nrp[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int n = nrow0 - nrs.first + slot + 4 * r;
+                    const int nl = nrow0 - nrs.first + lslot + 4 * r;
+                    nok[r] = nl < p.N;
+                    nrp[r] = nrs.codes + static_cast<size_t>(nok[r] ? nl : 0) * p.row_words;
+                    snext[r] = n < p.N ? bf16_bits_to_f32(__ldg(nrs.scales + n)) : 0.0f;
+                }
+                load_block_group<KB, R>(nrp, nok, 0, lg, cw);
+            }
         }
 
         if (live && seg_end) {
