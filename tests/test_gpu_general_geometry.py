@@ -70,9 +70,9 @@ def test_gemm_general_geometry(tq, oracle_lib, k, L, M):
 
 @pytest.mark.parametrize("k,L,M", [(8, 16, 15), (4, 16, 16), (6, 20, 16), (7, 12, 16), (8, 9, 14)])
 def test_gemm_general_two_row_shapes(tq, oracle_lib, k, L, M):
-    """The general-geometry shapes with two rows a lane (M = 15 at k = 8; M = 16
-    at k = 4, 6, 7), next to a three-row one, on several tile-groups, a ragged N
-    and K-ranges split over CTAs."""
+    """General-geometry shapes at the top of the small-M range (M = 14 .. 16, the
+    most registers a lane, and the shapes that once ran two rows a lane), on
+    several tile-groups, a ragged N and K-ranges split over CTAs."""
     N, K = 1001, 2048
     x, codes, scales = _inputs(M, K, N, k, seed=9000 + 17 * M + k + L)
     got = host_bits(tq.gemm(dev_bf16(x), dev_codes(codes), dev_bf16(scales), k, L=L))

@@ -161,16 +161,16 @@ struct SmallMDefault {
     using two = SmallMCfg<MM, 3, TMP ? 16 : KWARPS, true, 1, UB, GM, KET, true, TMP>;
     // any other (k, L): the quotient table only holds the byte sums that
     // 12-bit windows reach, so these compute the quotient, which needs more
-    // registers: 8 warps (255 registers a thread) from M = 6 up, and 2 rows a
-    // lane where 3 spill heavily at k words a group and measured slower
-    // (M = 15 with k = 8; M = 16 with k = 4, 6, 7; A/B on one GB300 at
-    // K = 5120, N = 17408)
-    static constexpr int GWARPS = (MM <= 2) ? 16 : (MM <= 5 ? 12 : 8);
-    static constexpr int general_rows(int kb) {
-        return ((MM == 15 && kb == 8) || (MM == 16 && (kb == 4 || kb == 6 || kb == 7))) ? 2 : 3;
-    }
+    // registers.  With activation-row pairs (from M = 3): 16 warps up to
+    // M = 10, 12 above; with k-pairs (M = 1, 2) 16.  A/B on one GB300 at
+    // K = 5120, N = 17408 against k-pairs at 8 warps (2 rows a lane for M = 15,
+    // k = 8 and M = 16, k = 4, 6, 7, where 3 spilled heavily), us: M = 8 k = 3
+    // L = 16 59.5 -> 55.4, M = 8 k = 8 L = 16 62.5 -> 60.6, M = 12 k = 3 L = 16
+    // 74.6 -> 70.7, M = 15 k = 4 L = 16 85.7 -> 80.7, M = 15 k = 8 L = 16
+    // 90.5 -> 85.6, M = 5 k = 5 L = 20 49.2 -> 49.9.
+    static constexpr int GWARPS = MPD ? (MM <= 10 ? 16 : 12) : 16;
     template <int KB>
-    using general = SmallMCfg<MM, general_rows(KB), GWARPS, false, 1, UB, GM, KET>;
+    using general = SmallMCfg<MM, 3, GWARPS, false, 1, UB, GM, false, false, MPD>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
 
