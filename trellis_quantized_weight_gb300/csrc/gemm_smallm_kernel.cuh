@@ -829,14 +829,15 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         peek = __shfl_sync(0xffffffffu, peek, 0);
         const bool by_peek = C::ET && has_last && peek == lneed;   // every other contributor is done
         const bool skip0 = by_peek && !pend1;                      // slot 0 is that segment
-        __syncwarp();   // the slot lanes' partial-sum stores are ordered before lane 0's tickets
+        __syncwarp();   // the slot lanes' partial-sum stores are ordered before the tickets
         uint32_t e0 = 0, e1 = 0;
-        if (lane == 0) {
-            if (pend0 && !tk_taken && !skip0) e0 = take_ticket(p.counters + ptg0 * WARPS + warp);
-            if (pend1 && !by_peek) e1 = take_ticket(p.counters + ptg1 * WARPS + warp);
-        }
-        e0 = __shfl_sync(0xffffffffu, e0, 0);
-        e1 = __shfl_sync(0xffffffffu, e1, 0);
+        // one atomic instruction for both tickets: lane 0 takes slot 0's,
+        // lane 1 slot 1's (two instructions would each wait for the other)
+        const bool tk_mine = lane == 0 ? (pend0 && !tk_taken && !skip0) : (lane == 1 && pend1 && !by_peek);
+        uint32_t ev = 0;
+        if (tk_mine) ev = take_ticket(p.counters + (lane == 0 ? ptg0 : ptg1) * WARPS + warp);
+        e0 = __shfl_sync(0xffffffffu, ev, 0);
+        e1 = __shfl_sync(0xffffffffu, ev, 1);
         const uint32_t t0 = __shfl_sync(0xffffffffu, tk0, 0);
         const uint32_t need0 = static_cast<uint32_t>(info_last(pinfo0) - info_first(pinfo0));
         const uint32_t need1 = static_cast<uint32_t>(info_last(pinfo1) - info_first(pinfo1));
@@ -845,7 +846,12 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         const int tgs[2] = {ptg0, ptg1};
         const uint32_t infos[2] = {pinfo0, pinfo1};
         if (use[0] || use[1]) {
-            fence_acq_rel_gpu();   // acquire: the other contributors' partial sums are visible
+            // A ticket taken here is an acq_rel atomic: its acquire, then the
+            // warp barrier, order the other contributors' partial sums before
+            // every lane's loads.  A count read relaxed (the in-loop ticket or
+            // the peek) needs the acquire fence.
+            if (by_peek || (use[0] && tk_taken))
+                fence_acq_rel_gpu();
             __syncwarp();
             reduce_split_tiles<C>(p, use, tgs, infos, warp, lane, out);
         }
