@@ -53,20 +53,28 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
-    """Compile and link the library if any source or header is newer than it."""
+def build(force: bool = False, verbose: bool = False, jobs: int | None = None,
+          defines: tuple[str, ...] = (), build_dir: str | None = None) -> str:
+    """Compile and link the library if any source or header is newer than it.
+
+    ``defines`` (nvcc -D) with a separate ``build_dir`` make another copy of the
+    library, e.g. the trace build (``TRELLIS_TRACE``, see trace.py); the shipped
+    library is the one built with neither."""
     home = cuda_home()
     nvcc = os.path.join(home, "bin", "nvcc")
-    os.makedirs(os.path.join(BUILD, "obj"), exist_ok=True)
+    out_dir = build_dir or BUILD
+    lib_path = os.path.join(out_dir, LIB_NAME)
+    flags = [*NVCC_FLAGS, *(f"-D{d}" for d in defines)]
+    os.makedirs(os.path.join(out_dir, "obj"), exist_ok=True)
     srcs = sources()
     headers = _headers()
-    objs = [os.path.join(BUILD, "obj", os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out_dir, "obj", os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def compile_one(src_obj):
         src, obj = src_obj
         if not force and not _stale(obj, [src] + headers):
             return None
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj + ".tmp"]
+        cmd = [nvcc, *ARCH, *flags, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj + ".tmp"]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -81,15 +89,15 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
             if out:
                 print(out)
 
-    if force or _stale(LIB_PATH, objs):
+    if force or _stale(lib_path, objs):
         libdir = os.path.join(home, "lib64")
-        cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", LIB_PATH + ".tmp", *objs,
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", lib_path + ".tmp", *objs,
                "-Xlinker", f"-rpath,{libdir}"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(LIB_PATH + ".tmp", LIB_PATH)
-    return LIB_PATH
+        os.replace(lib_path + ".tmp", lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

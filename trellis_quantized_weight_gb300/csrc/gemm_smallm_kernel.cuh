@@ -77,7 +77,32 @@ struct SmallMPlan {
     float* partials;    // workspace: [P][2][WARPS][R*M*4] fp32
     uint32_t* counters; // workspace: [ntg * WARPS]
     uint32_t lmask;     // 2^L - 1: the window mask of kernels built for a run-time L
+#ifdef TRELLIS_TRACE
+    unsigned long long* trace;   // trace build only: phase stamps (see trace_stamp)
+    size_t trace_words;
+#endif
 };
+
+// Trace build only (-DTRELLIS_TRACE; the shipped library is built without it):
+// clock64 stamps of the kernel's phases.  CTA c owns kTraceCtaWords words from
+// c * kTraceCtaWords: [0] SM id, [1] entry, [2] thread 0 leaving the loop,
+// [3] units; warp w's record of 8 words at 8 + 8w: [0] leaving the loop,
+// [1] tickets answered, [2] the reduction's partial sums loaded and added,
+// [3] done, [4] flags (bit 0/1: split first/last segment, bit 2: in-loop
+// ticket, bit 3/4: this warp reduced that tile).  Writes past the attached
+// buffer are dropped.
+#ifdef TRELLIS_TRACE
+constexpr int kTraceCtaWords = 8 + 8 * 16;
+__device__ __forceinline__ unsigned long long trace_clock() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void trace_stamp(const SmallMPlan& p, int c, int idx, unsigned long long v) {
+    const size_t i = static_cast<size_t>(c) * kTraceCtaWords + idx;
+    if (p.trace != nullptr && i < p.trace_words) p.trace[i] = v;
+}
+#endif
 
 // Compile-time shape of one instantiation.
 //   R      rows per lane (a warp's tile is 4*R rows)
@@ -333,7 +358,7 @@ __device__ __forceinline__ int info_slot(uint32_t info) { return static_cast<int
 template <class C>
 __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bool (&use)[2], const int (&tgs)[2],
                                                    const uint32_t (&infos)[2], int warp, int lane,
-                                                   uint16_t* __restrict__ out) {
+                                                   uint16_t* __restrict__ out, int c) {
     constexpr int MM = C::MM, WARPS = C::WARPS;
     constexpr int E = C::R * MM * 4;                  // sums of one warp's tile
     constexpr int EP = (E + 31) / 32;                 // sums per lane
@@ -375,6 +400,19 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
 #pragma unroll
                     for (int ep = 0; ep < EP; ++ep) sum[t][ep] = __fadd_rn(sum[t][ep], part[t][ep][i]);
     }
+#ifdef TRELLIS_TRACE
+    {
+        // stamped once every sum is complete (the clock read depends on them)
+        float z = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int ep = 0; ep < EP; ++ep) z += sum[t][ep];
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%clock64;" : "=l"(t) : "f"(z));
+        if (lane == 0) trace_stamp(p, c, 8 + 8 * warp + 2, t);
+    }
+#endif
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         if (!use[t]) continue;
@@ -408,6 +446,14 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
     float* xs = reinterpret_cast<float*>(smem_raw + C::TABLE_BYTES);   // C::RING slots of XS_UNIT floats
 
     const int c = blockIdx.x;
+#ifdef TRELLIS_TRACE
+    if (threadIdx.x == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        trace_stamp(p, c, 0, smid);
+        trace_stamp(p, c, 1, trace_clock());
+    }
+#endif
     const int u0 = unit_begin(c, p);
     const int u1 = unit_begin(c + 1, p);
     const int tid = threadIdx.x;
@@ -818,6 +864,18 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
 
     // the next grid on the stream may be scheduled as this CTA's SM frees up
     griddep_launch_dependents();
+#ifdef TRELLIS_TRACE
+    if (tid == 0) {
+        trace_stamp(p, c, 2, trace_clock());
+        trace_stamp(p, c, 3, static_cast<unsigned long long>(nunits));
+    }
+    if (lane == 0) {
+        trace_stamp(p, c, 8 + 8 * warp, trace_clock());
+        trace_stamp(p, c, 8 + 8 * warp + 1, 0);
+        trace_stamp(p, c, 8 + 8 * warp + 2, 0);
+        trace_stamp(p, c, 8 + 8 * warp + 4, 0);
+    }
+#endif
 
     // ---- the last contributor of a split tile reduces it ----
     if (pend0 || pend1) {
@@ -838,6 +896,9 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
         if (tk_mine) ev = take_ticket(p.counters + (lane == 0 ? ptg0 : ptg1) * WARPS + warp);
         e0 = __shfl_sync(0xffffffffu, ev, 0);
         e1 = __shfl_sync(0xffffffffu, ev, 1);
+#ifdef TRELLIS_TRACE
+        if (lane == 0) trace_stamp(p, c, 8 + 8 * warp + 1, trace_clock());
+#endif
         const uint32_t t0 = __shfl_sync(0xffffffffu, tk0, 0);
         const uint32_t need0 = static_cast<uint32_t>(info_last(pinfo0) - info_first(pinfo0));
         const uint32_t need1 = static_cast<uint32_t>(info_last(pinfo1) - info_first(pinfo1));
@@ -853,9 +914,18 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
             if (by_peek || (use[0] && tk_taken))
                 fence_acq_rel_gpu();
             __syncwarp();
-            reduce_split_tiles<C>(p, use, tgs, infos, warp, lane, out);
+            reduce_split_tiles<C>(p, use, tgs, infos, warp, lane, out, c);
         }
+#ifdef TRELLIS_TRACE
+        if (lane == 0)
+            trace_stamp(p, c, 8 + 8 * warp + 4,
+                        (pend0 ? 1u : 0u) | (pend1 ? 2u : 0u) | (tk_taken ? 4u : 0u) | (use[0] ? 8u : 0u) |
+                            (use[1] ? 16u : 0u));
+#endif
     }
+#ifdef TRELLIS_TRACE
+    if (lane == 0) trace_stamp(p, c, 8 + 8 * warp + 3, trace_clock());
+#endif
 }
 
 // Workspace layout: a fixed-capacity counter region at offset 0 (the same
@@ -920,6 +990,9 @@ int launch_smallm_instance(const uint16_t* x, const uint32_t* codes, const uint1
     if (ws_bytes < need || ws == nullptr) return -7;
     p.counters = static_cast<uint32_t*>(ws);
     p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+#ifdef TRELLIS_TRACE
+    p.trace = trace_buffer(&p.trace_words);
+#endif
     const size_t smem = C::SMEM_BYTES;
     static std::atomic<unsigned long long> opted{0};
     if (!smem_opt_in(gemm_smallm_kernel<C, KB, LL>, static_cast<int>(C::SMEM_BYTES), opted)) return -5;

@@ -19,6 +19,12 @@ constexpr int kT_abi = 256;
 constexpr int kMinK = 1, kMaxK = 8, kMaxL = 24;
 inline bool fast_geometry(int k, int L) { return L == 12 && k >= 2 && k <= 4; }
 
+#ifdef TRELLIS_TRACE
+// Trace build only: the device buffer the small-M kernels stamp their phases
+// into (null until trellis_trace_attach), and its size in 64-bit words.
+unsigned long long* trace_buffer(size_t* words);
+#endif
+
 struct DeviceInfo {
     int device = 0;
     int num_sms = 0;

@@ -232,3 +232,27 @@ int trellis_device_status(cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+#ifdef TRELLIS_TRACE
+// Trace build only (not declared in include/trellis.h and absent from the
+// shipped library): attach a device buffer of `bytes` that the small-M
+// kernels fill with clock64 stamps of their phases (layout beside
+// kTraceCtaWords in gemm_smallm_kernel.cuh); NULL detaches.
+namespace {
+unsigned long long* g_trace = nullptr;
+size_t g_trace_words = 0;
+}  // namespace
+
+namespace trellis {
+unsigned long long* trace_buffer(size_t* words) {
+    *words = g_trace_words;
+    return g_trace;
+}
+}  // namespace trellis
+
+extern "C" __attribute__((visibility("default"))) int trellis_trace_attach(void* buffer, size_t bytes) {
+    g_trace = static_cast<unsigned long long*>(buffer);
+    g_trace_words = buffer != nullptr ? bytes / sizeof(unsigned long long) : 0;
+    return TRELLIS_OK;
+}
+#endif
