@@ -423,9 +423,9 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
         for (int ep = 0; ep < EP; ++ep) {
             const int e = lane + 32 * ep;
             if (e < E) {
-                const int q = e & 3, rm = e >> 2;
-                const int r = rm / MM, m = rm - r * MM;
-                const int n = row0 - rs.first + q + 4 * r;
+                // e = m * 4R + (4r + q): the tile's 4R columns of row m are adjacent
+                const int m = e / (4 * C::R), col = e - m * (4 * C::R);
+                const int n = row0 - rs.first + col;
                 if (n < p.N) rs.out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum[t][ep]);
             }
         }
@@ -816,13 +816,33 @@ gemm_smallm_kernel(const uint16_t* __restrict__ x, const uint32_t* __restrict__ 
                 }
             } else {
                 // ---- split row: publish the partial now, take the ticket after the loop ----
-                // value (r, m) of row slot q sits at [(r*MM + m)*4 + q]
+                // value (r, m) of row slot q sits at [(m*R + r)*4 + q]: row m's 4R
+                // columns of the tile are adjacent, for the reduction's loads and stores
                 const int pslot = (tg == first_tg) ? 0 : 1;
                 float* mine = p.partials + ((static_cast<size_t>(c) * 2 + pslot) * WARPS + warp) * (R * MM * 4);
+                if constexpr (C::LUT) {
 #pragma unroll
-                for (int j = 0; j < NV / 8; ++j) {
-                    const int i = vbase + j;
-                    if (i < R * MM) mine[i * 4 + slot] = v[j];
+                    for (int j = 0; j < NV / 8; ++j) {
+                        const int i = vbase + j;
+                        if (i < R * MM) {
+                            const int r = i / MM, m = i - r * MM;
+                            mine[(m * R + r) * 4 + slot] = v[j];
+                        }
+                    }
+                } else {
+                    // the same positions with (r, m) stepped along j: fewer live
+                    // registers, which the run-time-window kernels need (M = 15,
+                    // k = 8, L = 16: 87.5 -> 85.8 us; the fast-geometry kernels
+                    // measured slower with it)
+                    int r = vbase / MM, m = vbase - r * MM;
+#pragma unroll
+                    for (int j = 0; j < NV / 8; ++j) {
+                        if (vbase + j < R * MM) mine[(m * R + r) * 4 + slot] = v[j];
+                        if (++m == MM) {
+                            m = 0;
+                            ++r;
+                        }
+                    }
                 }
                 if (pslot == 0) {
                     pend0 = true;
