@@ -51,6 +51,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include "kernels.h"
 #include "trellis_device.cuh"
@@ -149,6 +150,12 @@ struct SmallMCfg {
     static constexpr bool ET = ET_;
     static constexpr bool TWO = TWO_;
     static constexpr int GROUP_STRIDE = GM ? 4 : 1;  // lane distance between groups of a slot
+    // Split-K reduction form: 2 = a lane takes pairs of adjacent columns and
+    // loads 4 contributors a round; 1 = single columns, 4 a round; 0 = single
+    // columns, 8 a round.  The reduction is inlined into the kernel and moves
+    // the register allocation of its loop, so the form is chosen per shape by
+    // timing (fast-geometry single-matrix kernels; the others keep form 0).
+    static constexpr int RED = (!LUT || TWO || MM == 1) ? 0 : ((MM == 11 || MM == 15) ? 1 : 2);
 };
 
 // The shape used by the library for each M, chosen by timing back-to-back
@@ -361,7 +368,11 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
                                                    uint16_t* __restrict__ out, int c) {
     constexpr int MM = C::MM, WARPS = C::WARPS;
     constexpr int E = C::R * MM * 4;                  // sums of one warp's tile
-    constexpr int EP = (E + 31) / 32;                 // sums per lane
+    constexpr int V = C::RED == 2 ? 2 : 1;            // adjacent columns a lane takes at once
+    constexpr int EV = E / V;                         // ... as that many units (E is a multiple of 4)
+    constexpr int EP = (EV + 31) / 32;                // units per lane
+    constexpr int CR = C::RED == 0 ? 8 : 4;           // contributors loaded per round
+    using VT = typename std::conditional<V == 2, float2, float>::type;
     int c_first[2], c_last[2], cf_slot[2];
     int rounds = 0;
 #pragma unroll
@@ -369,36 +380,47 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
         c_first[t] = use[t] ? info_first(infos[t]) : 1;
         c_last[t] = use[t] ? info_last(infos[t]) : 0;
         cf_slot[t] = use[t] ? info_slot(infos[t]) : 0;
-        const int r = (c_last[t] - c_first[t] + 8) >> 3;
+        const int r = (c_last[t] - c_first[t] + CR) / CR;
         rounds = r > rounds ? r : rounds;
     }
-    float sum[2][EP];
+    float sum[2][EP][V];
 #pragma unroll
     for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int ep = 0; ep < EP; ++ep) sum[t][ep] = 0.0f;
+        for (int ep = 0; ep < EP; ++ep)
+#pragma unroll
+            for (int h = 0; h < V; ++h) sum[t][ep][h] = 0.0f;
     for (int rd = 0; rd < rounds; ++rd) {
-        float part[2][EP][8];
+        VT part[2][EP][CR];
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int cc = c_first[t] + 8 * rd + i;
+            for (int i = 0; i < CR; ++i) {
+                const int cc = c_first[t] + CR * rd + i;
                 const int cs = (cc == c_first[t]) ? cf_slot[t] : 0;
-                const float* src = p.partials + ((static_cast<size_t>(cc) * 2 + cs) * WARPS + warp) * E;
+                const VT* src = reinterpret_cast<const VT*>(
+                    p.partials + ((static_cast<size_t>(cc) * 2 + cs) * WARPS + warp) * E);
 #pragma unroll
                 for (int ep = 0; ep < EP; ++ep) {
-                    const int e = lane + 32 * ep;
-                    part[t][ep][i] = (cc <= c_last[t] && e < E) ? __ldcg(src + e) : 0.0f;
+                    const int ev = lane + 32 * ep;
+                    part[t][ep][i] = (cc <= c_last[t] && ev < EV) ? __ldcg(src + ev) : VT{};
                 }
             }
+        // contributors in CTA order, so the sums are the same whatever the form
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (c_first[t] + 8 * rd + i <= c_last[t])
+            for (int i = 0; i < CR; ++i)
+                if (c_first[t] + CR * rd + i <= c_last[t])
 #pragma unroll
-                    for (int ep = 0; ep < EP; ++ep) sum[t][ep] = __fadd_rn(sum[t][ep], part[t][ep][i]);
+                    for (int ep = 0; ep < EP; ++ep) {
+                        if constexpr (V == 2) {
+                            sum[t][ep][0] = __fadd_rn(sum[t][ep][0], part[t][ep][i].x);
+                            sum[t][ep][1] = __fadd_rn(sum[t][ep][1], part[t][ep][i].y);
+                        } else {
+                            sum[t][ep][0] = __fadd_rn(sum[t][ep][0], part[t][ep][i]);
+                        }
+                    }
     }
 #ifdef TRELLIS_TRACE
     {
@@ -407,7 +429,9 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int ep = 0; ep < EP; ++ep) z += sum[t][ep];
+            for (int ep = 0; ep < EP; ++ep)
+#pragma unroll
+                for (int h = 0; h < V; ++h) z += sum[t][ep][h];
         unsigned long long t;
         asm volatile("mov.u64 %0, %%clock64;" : "=l"(t) : "f"(z));
         if (lane == 0) trace_stamp(p, c, 8 + 8 * warp + 2, t);
@@ -421,12 +445,24 @@ __device__ __forceinline__ void reduce_split_tiles(const SmallMPlan& p, const bo
         const RowSrc rs = row_source<C>(p, nullptr, nullptr, out, row0);
 #pragma unroll
         for (int ep = 0; ep < EP; ++ep) {
-            const int e = lane + 32 * ep;
-            if (e < E) {
-                // e = m * 4R + (4r + q): the tile's 4R columns of row m are adjacent
+            const int ev = lane + 32 * ep;
+            if (ev < EV) {
+                // e = m * 4R + (4r + q): the tile's 4R columns of row m are
+                // adjacent (a pair never crosses a row: 4R is even)
+                const int e = V * ev;
                 const int m = e / (4 * C::R), col = e - m * (4 * C::R);
                 const int n = row0 - rs.first + col;
-                if (n < p.N) rs.out[static_cast<size_t>(m) * p.N + n] = bf16_bits_rn(sum[t][ep]);
+                uint16_t* dst = rs.out + static_cast<size_t>(m) * p.N + n;
+                if constexpr (V == 2) {
+                    if (n + 1 < p.N && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(sum[t][ep][0], sum[t][ep][1]);
+                    } else {
+                        if (n < p.N) dst[0] = bf16_bits_rn(sum[t][ep][0]);
+                        if (n + 1 < p.N) dst[1] = bf16_bits_rn(sum[t][ep][1]);
+                    }
+                } else {
+                    if (n < p.N) *dst = bf16_bits_rn(sum[t][ep][0]);
+                }
             }
         }
         if (lane == 0) p.counters[tile] = 0u;
