@@ -154,8 +154,8 @@ struct SmallMCfg {
     // loads 4 contributors a round; 1 = single columns, 4 a round; 0 = single
     // columns, 8 a round.  The reduction is inlined into the kernel and moves
     // the register allocation of its loop, so the form is chosen per shape by
-    // timing (fast-geometry single-matrix kernels; the others keep form 0).
-    static constexpr int RED = (!LUT || TWO || MM == 1) ? 0 : ((MM == 11 || MM == 15) ? 1 : 2);
+    // timing (single-matrix kernels; gate/up keeps form 0).
+    static constexpr int RED = (TWO || MM == 1) ? 0 : ((MM == 11 || MM == 15) ? 1 : 2);
 };
 
 // The shape used by the library for each M, chosen by timing back-to-back
