@@ -172,16 +172,18 @@ struct SmallMDefault {
     // 5 42.8 -> 41.2, 6 47.3 -> 43.8, 7 52.3 -> 50.0, 8 54.5 -> 50.3,
     // 9 59.6 -> 57.2, 10 64.7 -> 58.8 (16 warps); 11 69.5 -> 67.9, 12 69.6 ->
     // 64.2, 13 72.1 -> 69.5, 15 78.7 -> 76.7, 16 82.0 -> 79.4 (12 warps; 16
-    // spilled and measured slower at M = 11, 12); 14 77.2 -> 72.7 (8 warps).
+    // spilled and measured slower at M = 11, 12); 14 77.2 -> 72.7 (8 warps,
+    // then 12 once the split-K tail got shorter: k = 4 72.9 -> 70.3, k = 3
+    // 78.0 -> 74.2, k = 2 71.5 -> 69.3).
     // M = 1, 2 keep k-pairs (a pair of rows would leave half of each FMA idle).
     static constexpr bool MPD = MM >= 3;
     static constexpr int KWARPS = (MM <= 2) ? 16 : (MM <= 10 ? 12 : 8);   // with k-pairs
-    static constexpr int WARPS = MPD ? (MM <= 10 ? 16 : (MM == 14 ? 8 : 12)) : KWARPS;
+    static constexpr int WARPS = MPD ? (MM <= 10 ? 16 : 12) : KWARPS;
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
     static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
-    // early tickets for M >= 12 at 8 warps; off at 12 (M = 12 64.3 -> 63.1 us,
-    // 13 69.6 -> 68.7, 15 76.7 -> 75.7, 16 79.5 -> 78.9; M = 14 at 8 warps
-    // 72.7 with them, 76.7 without)
+    // early tickets only at 8 warps (the gate/up k-pair kernels of M >= 12);
+    // off at 12 (M = 12 64.3 -> 63.1 us, 13 69.6 -> 68.7, 15 76.7 -> 75.7,
+    // 16 79.5 -> 78.9; M = 14 at 8 warps 72.7 with them, 76.7 without)
     static constexpr bool ET = MM >= 12 && WARPS == 8;
     static constexpr bool KET = MM >= 12;   // with k-pairs (8 warps)
     using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, false, MPD>;
