@@ -181,18 +181,17 @@ struct SmallMDefault {
     static constexpr int WARPS = MPD ? (MM <= 10 ? 16 : 12) : KWARPS;
     static constexpr int UB = (MM <= 2) ? 3 : (MM <= 11) ? 4 : 3;
     static constexpr bool GM = MM >= 6;   // activation traffic matters more than the shuffles
-    // early tickets only at 8 warps (the gate/up k-pair kernels of M >= 12);
-    // off at 12 (M = 12 64.3 -> 63.1 us, 13 69.6 -> 68.7, 15 76.7 -> 75.7,
-    // 16 79.5 -> 78.9; M = 14 at 8 warps 72.7 with them, 76.7 without)
+    // early tickets (8 warps only) measured slower at 12 warps (M = 12 64.3
+    // -> 63.1 us without, 13 69.6 -> 68.7, 15 76.7 -> 75.7, 16 79.5 -> 78.9);
+    // no default shape runs 8 warps any more
     static constexpr bool ET = MM >= 12 && WARPS == 8;
-    static constexpr bool KET = MM >= 12;   // with k-pairs (8 warps)
     using type = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, ET, false, MPD>;
-    // gate and up: activation-row pairs at 16 warps for M = 3 .. 10 (M = 5
-    // 94.2 -> 85.1 us, M = 8 117.3 -> 103.3 at K = 5120, N = 17408, measured
-    // with both on a slower build); k-pairs above (the 12-warp pairs measured
-    // slower there: M = 12 141.1 -> 145.7, M = 15 156.3 -> 161.7)
-    static constexpr bool TMP = MM >= 3 && MM <= 10;
-    using two = SmallMCfg<MM, 3, TMP ? 16 : KWARPS, true, 1, UB, GM, KET, true, TMP>;
+    // gate and up: activation-row pairs as above (M = 5 94.2 -> 85.1 us,
+    // M = 8 117.3 -> 103.3 at K = 5120, N = 17408 against k-pairs at 12 warps,
+    // measured with both on a slower build; M = 12 141.4 -> 123.8, M = 15
+    // 158.0 -> 147.1 against k-pairs at 8 warps with early tickets, once the
+    // split-K tail got shorter)
+    using two = SmallMCfg<MM, 3, WARPS, true, 1, UB, GM, false, true, MPD>;
     // any other (k, L): the quotient table only holds the byte sums that
     // 12-bit windows reach, so these compute the quotient, which needs more
     // registers.  With activation-row pairs (from M = 3): 16 warps up to
