@@ -160,9 +160,10 @@ struct SmallMCfg {
 
 // The shape used by the library for each M, chosen by timing back-to-back
 // calls of the M = 1, 5, 8 and 15 workloads on GB300 over R, WARPS, UB, LUT and
-// CTAs per SM (M in between takes its neighbours' shape).  M = 11 takes 8 warps:
-// at 12 warps its registers (168 a thread) spill, and 8 warps measured 7-12%
-// faster; M = 9 and 10 measured the same or faster at 12.
+// CTAs per SM (M in between takes its neighbours' shape).  With k-pairs (now
+// M = 1, 2 only, KWARPS) M = 11 took 8 warps: at 12 its registers (168 a
+// thread) spilled, and 8 measured 7-12% faster; M = 9 and 10 measured the
+// same or faster at 12.  With activation-row pairs every M >= 11 fits 12.
 template <int MM>
 struct SmallMDefault {
     // Pairs of activation rows per f32x2 FMA (MP) from M = 3, an odd M's last
