@@ -201,10 +201,13 @@ struct SmallMDefault {
     // k = 8 and M = 16, k = 4, 6, 7, where 3 spilled heavily), us: M = 8 k = 3
     // L = 16 59.5 -> 55.4, M = 8 k = 8 L = 16 62.5 -> 60.6, M = 12 k = 3 L = 16
     // 74.6 -> 70.7, M = 15 k = 4 L = 16 85.7 -> 80.7, M = 15 k = 8 L = 16
-    // 90.5 -> 85.6, M = 5 k = 5 L = 20 49.2 -> 49.9.
+    // 90.5 -> 85.6, M = 5 k = 5 L = 20 49.2 -> 49.9.  At k = 8 the 16-warp
+    // shapes of M = 6 .. 10 spill 116-286 bytes and 12 warps none: M = 8
+    // 59.6 -> 55.7 us (at M = 15, 8 warps instead of 12 measured 84.9 -> 86.8).
     static constexpr int GWARPS = MPD ? (MM <= 10 ? 16 : 12) : 16;
     template <int KB>
-    using general = SmallMCfg<MM, 3, GWARPS, false, 1, UB, GM, false, false, MPD>;
+    using general = SmallMCfg<MM, 3, (KB == 8 && MM >= 6 && MM <= 10) ? 12 : GWARPS, false, 1, UB, GM, false,
+                              false, MPD>;
     static_assert(type::SMEM_BYTES <= 232448, "shared memory per CTA exceeds 227 KB");
 };
 
