@@ -141,8 +141,8 @@ TRELLIS_API int trellis_decode(const uint32_t *codes, const uint16_t *scales, in
  * region: calls that may overlap on the GPU (on two streams) race; use
  * trellis_gemm_ws with a workspace per stream for concurrent calls.
  * Errors: as trellis_decode, plus M outside 1..65536 -> TRELLIS_ERR_UNSUPPORTED;
- * on a device with more than 256 SMs the region is too small for M <= 16 ->
- * TRELLIS_ERR_WORKSPACE (use trellis_gemm_ws).
+ * on a device with more than 170 SMs the region is too small for some
+ * M <= 16 shapes -> TRELLIS_ERR_WORKSPACE (use trellis_gemm_ws).
  */
 TRELLIS_API int trellis_gemm(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M, int K,
                              int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);
@@ -250,10 +250,10 @@ TRELLIS_API int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, i
  *
  * The first call on each device does a one-time set-up with that device
  * current (it looks up the array's device address and clears its counter
- * region, synchronising the device); make that first call before any stream
- * capture.  Under the CUDA runtime's default lazy module loading, the array
- * and the kernels' code are placed in device memory when that first call
- * touches them, not when the library is loaded: a process that reserves all
+ * region, synchronising the device).  Under the CUDA runtime's default lazy
+ * module loading, the array and the kernels' code are placed in device memory
+ * when that first call touches them, not when the library is loaded: a
+ * process that reserves all
  * free device memory up front must make its first call (per device and per
  * bit width k, whose kernels are separate modules) before reserving, or run
  * with CUDA_MODULE_LOADING=EAGER.  Every call shares the array: calls that may
@@ -262,7 +262,7 @@ TRELLIS_API int trellis_gemm_gateup_workspace_size(int M, int K, int N, int k, i
  * trellis_gemm; then geometries whose scratch (as reported by
  * trellis_gemm_workspace_size) exceeds 16 MiB are rejected with
  * TRELLIS_ERR_WORKSPACE before any launch (a guard for devices with more than
- * 1280 SMs: below that the scratch of every accepted geometry fits).
+ * 853 SMs: below that the scratch of every accepted geometry fits).
  */
 TRELLIS_API int trellis_gemm_noalloc(const uint16_t *x, const uint32_t *codes, const uint16_t *scales, int M,
                                      int K, int N, int k, int L, int T, uint16_t *out, cudaStream_t stream);

@@ -76,8 +76,8 @@ extern "C" int trellis_gemm_noalloc(const uint16_t* x, const uint32_t* codes, co
     rc = trellis_gemm_workspace_size(M, K, N, k, L, T, &need);
     if (rc != TRELLIS_OK) return rc;
     // Beyond the fixed array.  Defensive: the scratch grows with the SM count
-    // (1 MiB of counters plus at most 12 KiB a CTA), so no accepted geometry
-    // exceeds 16 MiB on a device with at most 1280 SMs.
+    // (1 MiB of counters plus at most 18 KiB a CTA), so no accepted geometry
+    // exceeds 16 MiB on a device with at most 853 SMs.
     if (need > kNoAllocScratchBytes) return TRELLIS_ERR_WORKSPACE;
     if (M > 16) return trellis::launch_gemm_tc(x, codes, scales, M, K, N, k, L, out, stream);   // no scratch
     NoAllocDevice d;

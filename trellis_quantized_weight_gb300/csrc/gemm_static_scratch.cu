@@ -15,8 +15,9 @@
 //  * every trellis_gemm call on a device shares it, so calls that may overlap
 //    on the GPU race (trellis_gemm_ws with separate workspaces serves
 //    concurrent streams);
-//  * its size covers 1 MiB of counters plus 12 KiB of partial sums per SM for
-//    up to 256 SMs; a device with more SMs needs trellis_gemm_ws.
+//  * its size covers 1 MiB of counters plus up to 18 KiB of partial sums per SM
+//    (M = 16 at 12 warps) for up to 170 SMs; on a device with more SMs the
+//    shapes that need more are rejected, and trellis_gemm_ws serves them.
 #include <cstdint>
 #include <mutex>
 

@@ -163,7 +163,7 @@ int trellis_gemm(const uint16_t* x, const uint32_t* codes, const uint16_t* scale
     if (rc != TRELLIS_OK) return rc;
     const size_t need = trellis::gemm_smallm_workspace_bytes(M, K, N, k, L, dev);
     if (need == 0) return TRELLIS_ERR_SHAPE;
-    if (need > trellis::kGemmScratchBytes) return TRELLIS_ERR_WORKSPACE;   // more than 256 SMs
+    if (need > trellis::kGemmScratchBytes) return TRELLIS_ERR_WORKSPACE;   // more than 170 SMs
     void* ws = nullptr;
     rc = trellis::gemm_static_scratch(&ws);
     if (rc != TRELLIS_OK) return rc;
