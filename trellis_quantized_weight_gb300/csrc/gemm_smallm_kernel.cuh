@@ -33,11 +33,13 @@
 //    sums by butterfly shuffles (lane distances 4, 8, 16).  A row whose K-range is split over several
 //    CTAs writes fp32 partial sums to the workspace as soon as its segment
 //    ends; only a CTA's first and last segments can be split, and both take
-//    their per-tile tickets after the CTA's last unit, so the loop never waits
-//    on a fence or an atomic.  The last CTA to take a tile's ticket adds the
-//    partials in CTA order, rounds to bf16, stores and resets the counter.
-//    The sum order is fixed: identical inputs give identical bits.  No CTA
-//    ever waits on another.
+//    their per-tile tickets after the CTA's last unit (one atomic instruction
+//    for the two), so the loop never waits on a fence or an atomic.  The last
+//    CTA to take a tile's ticket adds the partials in CTA order, rounds to
+//    bf16, stores and resets the counter; partials are laid out [m][r][slot],
+//    so its loads and stores run along each output row's 4R columns.  The sum
+//    order is fixed: identical inputs give identical bits.  No CTA ever waits
+//    on another.
 //  * Decode per weight: funnel shift + mask, hash IMAD, then either the dp4a
 //    byte sum into a float and the two-op quotient (trellis_device.cuh), or one
 //    dp4a that turns the hash into the address of the quotient in a per-lane
